@@ -1,0 +1,389 @@
+// The C ABI declared in include/dg.h: argument checks, tile-shape choice, TMA descriptors, launch.
+//
+// Tile-shape choice follows the pages' "unaligned block sizes" and automatic block-size selection:
+// BN (the tile's N extent) is picked per problem from multiples of 32 up to 256 so that the number
+// of output tiles fills the SMs in as few, as full waves as possible.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "dg.h"
+#include "dg_launch.cuh"
+
+namespace dg {
+
+__device__ int g_status_word;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sms = 0;
+    int* status = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+dg_status device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DG_CUDA_ERROR;
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return DG_CUDA_ERROR;
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return DG_CUDA_ERROR;
+            d.status = static_cast<int*>(p);
+        }
+        d.ready = true;
+    }
+    *out = d;
+    return d.supported ? DG_OK : DG_NO_DEVICE_SUPPORT;
+}
+
+dg_status encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? DG_OK : DG_CUDA_ERROR;
+}
+
+// Row-major e4m3 matrix [rows, k] (k contiguous) read in boxes of box_rows x 128 with the 128-byte
+// swizzle the MMA descriptors expect.
+dg_status make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// BN candidates per layout; each must have a specialisation in the matching dg_inst_*.cu file.
+constexpr int kBnNormal[] = {64, 96, 128, 160, 192, 224, 256};
+constexpr int kBnContiguous[] = {128, 160, 192, 224, 256};
+constexpr int kBnMasked[] = {64, 128, 192, 256};
+constexpr int kBnKGrouped[] = {128};
+
+// Pick BN minimising waves * (BN + per-tile overhead), ties to the larger BN: the time of one wave of
+// 128 x BN tiles grows with BN, and the number of waves is the tile count over the SM count.
+template <size_t NC>
+int choose_bn(const int (&cands)[NC], int64_t row_blocks, int n, int sms) {
+    int best = cands[NC - 1];
+    int64_t best_cost = INT64_MAX;
+    for (size_t i = 0; i < NC; ++i) {
+        const int bn = cands[i];
+        const int64_t tiles = row_blocks * cdiv(n, bn);
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const int64_t cost = waves * (bn + 16);
+        if (cost <= best_cost) { best_cost = cost; best = bn; }
+    }
+    return best;
+}
+
+template <int MODE>
+cudaError_t launch_bn(int bn, const Launch& L);
+
+template <>
+cudaError_t launch_bn<kNormal>(int bn, const Launch& L) {
+    switch (bn) {
+        case 64: return launch<kNormal, 64>(L);
+        case 96: return launch<kNormal, 96>(L);
+        case 128: return launch<kNormal, 128>(L);
+        case 160: return launch<kNormal, 160>(L);
+        case 192: return launch<kNormal, 192>(L);
+        case 224: return launch<kNormal, 224>(L);
+        case 256: return launch<kNormal, 256>(L);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_bn<kContiguous>(int bn, const Launch& L) {
+    switch (bn) {
+        case 128: return launch<kContiguous, 128>(L);
+        case 160: return launch<kContiguous, 160>(L);
+        case 192: return launch<kContiguous, 192>(L);
+        case 224: return launch<kContiguous, 224>(L);
+        case 256: return launch<kContiguous, 256>(L);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_bn<kMasked>(int bn, const Launch& L) {
+    switch (bn) {
+        case 64: return launch<kMasked, 64>(L);
+        case 128: return launch<kMasked, 128>(L);
+        case 192: return launch<kMasked, 192>(L);
+        case 256: return launch<kMasked, 256>(L);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_bn<kKGrouped>(int bn, const Launch& L) {
+    switch (bn) {
+        case 128: return launch<kKGrouped, 128>(L);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Optional override of the tile width, for tuning sweeps only (DG_BN=<n>); ignored unless valid.
+template <size_t NC>
+int bn_override(const int (&cands)[NC], int chosen) {
+    const char* s = getenv("DG_BN");
+    if (!s) return chosen;
+    const int v = atoi(s);
+    for (size_t i = 0; i < NC; ++i)
+        if (cands[i] == v) return v;
+    return chosen;
+}
+
+dg_status common_prologue(DeviceInfo* dev) {
+    dg_status st = device_info(dev);
+    if (st != DG_OK) return st;
+    return encoder();
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+const char* dg_status_string(dg_status s) {
+    switch (s) {
+        case DG_OK: return "DG_OK";
+        case DG_INVALID_ARG: return "DG_INVALID_ARG";
+        case DG_UNSUPPORTED_SHAPE: return "DG_UNSUPPORTED_SHAPE";
+        case DG_MISALIGNED: return "DG_MISALIGNED";
+        case DG_CUDA_ERROR: return "DG_CUDA_ERROR";
+        case DG_NO_DEVICE_SUPPORT: return "DG_NO_DEVICE_SUPPORT";
+        case DG_DEVICE_TIMEOUT: return "DG_DEVICE_TIMEOUT";
+    }
+    return "DG_UNKNOWN_STATUS";
+}
+
+dg_status dg_device_status(cudaStream_t stream) {
+    DeviceInfo dev;
+    dg_status st = device_info(&dev);
+    if (st != DG_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DG_CUDA_ERROR;
+    int v = 0;
+    if (cudaMemcpy(&v, dev.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DG_CUDA_ERROR;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DG_CUDA_ERROR;
+        return DG_DEVICE_TIMEOUT;
+    }
+    return DG_OK;
+}
+
+dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
+                         int M, int N, int K, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
+    if (M == 0 || N == 0) return DG_OK;
+    if (!D) return DG_INVALID_ARG;
+    if (K % 128 != 0 || N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (!aligned(D, 16)) return DG_MISALIGNED;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+    if (K == 0)
+        return cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
+
+    const int bn = bn_override(kBnNormal, choose_bn(kBnNormal, cdiv(M, BM), N, dev.sms));
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if (make_operand_map(&L.tmap_a, A, M, K, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.status = dev.status;
+    p.rows = M;
+    p.n = N;
+    p.kbs = K / 128;
+    p.groups = 1;
+    p.sfb_rows = cdiv(N, 128);
+    p.m_blocks = cdiv(M, BM);
+    p.n_blocks = cdiv(N, bn);
+    const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
+    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = static_cast<int>(tiles);
+    L.grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    L.stream = stream;
+    return launch_bn<kNormal>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
+dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
+                                  const int32_t* m_indices, void* D, int Mt, int N, int K, int G,
+                                  cudaStream_t stream) {
+    if (Mt < 0 || N < 0 || K < 0 || G < 0) return DG_INVALID_ARG;
+    if (Mt == 0 || N == 0) return DG_OK;
+    if (G == 0) return DG_INVALID_ARG;
+    if (K % 128 != 0 || K == 0 || N % 8 != 0 || Mt % 128 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (!A || !B || !sfa || !sfb || !m_indices || !D) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(sfa, 4) || !aligned(sfb, 4) ||
+        !aligned(m_indices, 4))
+        return DG_MISALIGNED;
+    if (static_cast<int64_t>(G) * N > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+
+    const int bn = bn_override(kBnContiguous, choose_bn(kBnContiguous, cdiv(Mt, BM), N, dev.sms));
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if (make_operand_map(&L.tmap_a, A, Mt, K, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.m_indices = m_indices;
+    p.status = dev.status;
+    p.rows = Mt;
+    p.n = N;
+    p.kbs = K / 128;
+    p.groups = G;
+    p.sfb_rows = cdiv(N, 128);
+    p.m_blocks = Mt / BM;
+    p.n_blocks = cdiv(N, bn);
+    const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
+    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = static_cast<int>(tiles);
+    L.grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    L.stream = stream;
+    return launch_bn<kContiguous>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
+dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
+                              const int32_t* masked_m, void* D, int G, int max_m, int N, int K, int expected_m,
+                              cudaStream_t stream) {
+    if (G < 0 || max_m < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
+    if (G == 0 || max_m == 0 || N == 0) return DG_OK;
+    if (G > MAX_MASKED_G) return DG_INVALID_ARG;
+    if (K % 128 != 0 || K == 0 || N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (!A || !B || !sfa || !sfb || !masked_m || !D) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(sfa, 4) || !aligned(sfb, 4) ||
+        !aligned(masked_m, 4))
+        return DG_MISALIGNED;
+    if (static_cast<int64_t>(G) * max_m > INT32_MAX || static_cast<int64_t>(G) * N > INT32_MAX)
+        return DG_UNSUPPORTED_SHAPE;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+
+    const int hint = (expected_m > 0 && expected_m < max_m) ? expected_m : max_m;
+    const int bn = bn_override(kBnMasked, choose_bn(kBnMasked, static_cast<int64_t>(G) * cdiv(hint, BM), N, dev.sms));
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if (make_operand_map(&L.tmap_a, A, static_cast<int64_t>(G) * max_m, K, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.masked_m = masked_m;
+    p.status = dev.status;
+    p.rows = max_m;
+    p.n = N;
+    p.kbs = K / 128;
+    p.groups = G;
+    p.sfb_rows = cdiv(N, 128);
+    p.m_blocks = cdiv(max_m, BM);
+    p.n_blocks = cdiv(N, bn);
+    const int64_t max_tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
+    if (max_tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = 0;  // counted on the device from masked_m
+    L.grid = static_cast<int>(max_tiles < dev.sms ? max_tiles : dev.sms);
+    L.stream = stream;
+    return launch_bn<kMasked>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
+dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
+                             const int32_t* ks_host, float* D, int G, int M, int N, cudaStream_t stream) {
+    if (G < 0 || M < 0 || N < 0) return DG_INVALID_ARG;
+    if (G == 0 || M == 0 || N == 0) return DG_OK;
+    if (G > MAX_KGROUPS || !ks_host) return DG_INVALID_ARG;
+    int64_t sumK = 0;
+    for (int g = 0; g < G; ++g) {
+        if (ks_host[g] < 0) return DG_INVALID_ARG;
+        if (ks_host[g] % 128 != 0) return DG_UNSUPPORTED_SHAPE;
+        sumK += ks_host[g];
+    }
+    if (N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (sumK == 0) return DG_OK;
+    if (sumK > INT32_MAX || static_cast<int64_t>(G) * M > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    if (!A || !B || !sfa || !sfb || !D) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(sfa, 4) || !aligned(sfb, 4))
+        return DG_MISALIGNED;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+
+    const int bn = bn_override(kBnKGrouped, choose_bn(kBnKGrouped, static_cast<int64_t>(G) * cdiv(M, BM), N, dev.sms));
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if (make_operand_map(&L.tmap_a, A, M, sumK, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, sumK, bn) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.status = dev.status;
+    p.rows = M;
+    p.n = N;
+    p.kbs = static_cast<int>(sumK / 128);
+    p.groups = G;
+    p.sfb_rows = N;
+    p.m_blocks = cdiv(M, BM);
+    p.n_blocks = cdiv(N, bn);
+    int off = 0;
+    for (int g = 0; g < G; ++g) {
+        p.kb_off[g] = off;
+        off += ks_host[g] / 128;
+    }
+    p.kb_off[G] = off;
+    const int64_t tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
+    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = static_cast<int>(tiles);
+    L.grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    L.stream = stream;
+    return launch_bn<kKGrouped>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
+}  // extern "C"

@@ -1,0 +1,11 @@
+// Kernel specialisations of the contiguous layout (one translation unit per layout).
+#define DG_DEFINE_LAUNCH
+#include "dg_launch.cuh"
+
+namespace dg {
+template cudaError_t launch<kContiguous, 128>(const Launch&);
+template cudaError_t launch<kContiguous, 160>(const Launch&);
+template cudaError_t launch<kContiguous, 192>(const Launch&);
+template cudaError_t launch<kContiguous, 224>(const Launch&);
+template cudaError_t launch<kContiguous, 256>(const Launch&);
+}  // namespace dg

@@ -1,0 +1,7 @@
+// Kernel specialisations of the kgrouped layout (one translation unit per layout).
+#define DG_DEFINE_LAUNCH
+#include "dg_launch.cuh"
+
+namespace dg {
+template cudaError_t launch<kKGrouped, 128>(const Launch&);
+}  // namespace dg

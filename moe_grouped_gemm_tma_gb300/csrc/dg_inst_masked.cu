@@ -1,0 +1,10 @@
+// Kernel specialisations of the masked layout (one translation unit per layout).
+#define DG_DEFINE_LAUNCH
+#include "dg_launch.cuh"
+
+namespace dg {
+template cudaError_t launch<kMasked, 64>(const Launch&);
+template cudaError_t launch<kMasked, 128>(const Launch&);
+template cudaError_t launch<kMasked, 192>(const Launch&);
+template cudaError_t launch<kMasked, 256>(const Launch&);
+}  // namespace dg

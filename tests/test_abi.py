@@ -1,0 +1,73 @@
+"""The C ABI library builds, loads and exports every entry point that include/dg.h declares; argument
+checks that need no GPU reject bad calls before any CUDA work (CPU only)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import moe_grouped_gemm_tma_gb300 as dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dg.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:dg_status|const char\*)\s+(dg_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_four_operations():
+    syms = declared_symbols()
+    for s in ("dg_gemm_fp8_nt", "dg_m_grouped_contiguous", "dg_m_grouped_masked", "dg_k_grouped_wgrad",
+              "dg_status_string", "dg_device_status"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol():
+    L = dg.load()
+    for s in declared_symbols():
+        assert hasattr(L, s), s
+
+
+def test_python_binding_has_the_same_names():
+    for s in declared_symbols():
+        assert callable(getattr(dg, s)), s
+
+
+def test_status_strings():
+    assert dg.dg_status_string(0) == "DG_OK"
+    assert dg.dg_status_string(6) == "DG_DEVICE_TIMEOUT"
+    assert dg.dg_status_string(99) == "DG_UNKNOWN_STATUS"
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_rejects_bad_shapes_before_any_cuda_call():
+    L = dg.load()
+    ok = _fake(0x10000)
+    assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, ok, -1, 8, 128, None) == 1
+    assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, ok, 0, 8, 128, None) == 0          # empty: no-op
+    assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, ok, 4, 8, 100, None) == 2          # K % 128
+    assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, ok, 4, 12, 128, None) == 2         # N % 8
+    assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, _fake(0x10008), 4, 8, 128, None) == 3  # D misaligned
+    assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, None, 4, 8, 128, None) == 1
+    assert L.dg_m_grouped_contiguous(ok, ok, ok, ok, ok, ok, 100, 8, 128, 2, None) == 2  # Mt % 128
+    assert L.dg_m_grouped_contiguous(ok, ok, ok, ok, ok, ok, 128, 8, 128, 0, None) == 1  # G = 0
+    assert L.dg_m_grouped_masked(ok, ok, ok, ok, ok, ok, 2000, 64, 8, 128, 0, None) == 1  # G too large
+    assert L.dg_m_grouped_masked(ok, ok, ok, ok, ok, ok, 2, 64, 8, 130, 0, None) == 2
+    ks = (ctypes.c_int32 * 2)(128, 100)
+    assert L.dg_k_grouped_wgrad(ok, ok, ok, ok, ks, ok, 2, 8, 8, None) == 2   # ks % 128
+    ks = (ctypes.c_int32 * 2)(128, -128)
+    assert L.dg_k_grouped_wgrad(ok, ok, ok, ok, ks, ok, 2, 8, 8, None) == 1
+    ks = (ctypes.c_int32 * 2)(0, 0)
+    assert L.dg_k_grouped_wgrad(ok, ok, ok, ok, ks, ok, 2, 8, 8, None) == 0   # nothing to add
+
+
+def test_scale_shapes_follow_the_pages_usage_example():
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "page_usage_example.json")))
+    sfa, sfb = dg.scale_shapes(g["M"], g["N"], g["K"])
+    assert list(sfa) == g["sfa_shape"] and list(sfb) == g["sfb_shape"]

@@ -1,0 +1,99 @@
+"""GPU parity of the normal GEMM (dg_gemm_fp8_nt) against the CPU oracle on identical seeded inputs."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_tma_gb300 as dg
+from moe_grouped_gemm_tma_gb300 import inputs as I
+from oracle import oracle as O
+from tests.gpu_util import bf16_bits, bits_to_f64, check_bf16, dev, sample_rows, sentinel_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def run_normal(c, D=None):
+    if D is None:
+        D = sentinel_bf16(c.M, c.N)
+    dg.dg_gemm_fp8_nt(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), D)
+    assert dg.dg_device_status() == 0
+    return D
+
+
+def test_tiny_config_full_parity():
+    # the small workload: M=128, N=256, K=512
+    c = I.make_normal(I.seed_for(0), 128, 256, 512)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), "tiny")
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 256, 128), (64, 2112, 1024), (200, 2112, 768), (300, 1000, 384), (129, 4096, 256), (512, 7168, 2048),
+])
+def test_normal_shapes_full_parity(M, N, K):
+    c = I.make_normal(I.seed_for(1, M + N + K), M, N, K)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("bn", [64, 96, 128, 160, 192, 224, 256])
+def test_every_tile_width(bn, monkeypatch):
+    # ragged in M (two row blocks, the second partial) and in N for every BN
+    monkeypatch.setenv("DG_BN", str(bn))
+    c = I.make_normal(I.seed_for(1, 900 + bn), 200, 1000, 512)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn}")
+
+
+def test_integer_exact_bitwise():
+    # unit scales and values in {-1, 0, 1}: every output is an integer <= 256, exact in BF16
+    rng = np.random.default_rng(5)
+    M, N, K = 256, 512, 256
+    codes = np.array([0xB8, 0x00, 0x38], dtype=np.uint8)
+    A = torch.from_numpy(rng.choice(codes, size=(M, K)))
+    B = torch.from_numpy(rng.choice(codes, size=(N, K)))
+    sfa, sfb = torch.ones(M, K // 128), torch.ones(N // 128, K // 128)
+    D = sentinel_bf16(M, N)
+    dg.dg_gemm_fp8_nt(dev(A), dev(sfa), dev(B), dev(sfb), D)
+    assert dg.dg_device_status() == 0
+    np.testing.assert_array_equal(bf16_bits(D), O.gemm_fp8_nt(A, sfa, B, sfb))
+
+
+def test_pow2_scale_rules_bitwise():
+    c = I.make_normal(I.seed_for(1, 77), 256, 512, 512)
+    base = bits_to_f64(bf16_bits(run_normal(c)))
+    sfa = c.sfa.clone()
+    sfa[5] *= 8.0
+    sfb = c.sfb.clone()
+    sfb[2] *= 0.25
+    c2 = I.NormalCase(c.M, c.N, c.K, c.A, sfa, c.B, sfb)
+    got = bits_to_f64(bf16_bits(run_normal(c2)))
+    want = base.copy()
+    want[5] *= 8.0
+    want[:, 256:384] *= 0.25
+    np.testing.assert_array_equal(got, want)
+
+
+def test_k_zero_writes_zeros():
+    D = sentinel_bf16(4, 16)
+    e = torch.empty(0, dtype=torch.uint8, device="cuda")
+    s = torch.empty(0, dtype=torch.float32, device="cuda")
+    st = dg.load().dg_gemm_fp8_nt(e.data_ptr(), s.data_ptr(), e.data_ptr(), s.data_ptr(), D.data_ptr(), 4, 16, 0,
+                                  torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert (D.float() == 0).all()
+
+
+@pytest.mark.parametrize("N,K", [(2112, 7168), (24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048)])
+def test_dense_workload_sampled_rows(N, K):
+    # the dense workload at full size (M in {64, 128, 4096}), in the launch configuration the bench
+    # times; the oracle recomputes a sample of rows, including tile-boundary rows
+    big = I.make_normal(I.seed_for(1, 0), 4096, N, K)
+    for M in (64, 128, 4096):
+        c = I.NormalCase(M, N, K, big.A[:M], big.sfa[:M], big.B, big.sfb)
+        D = run_normal(c)
+        rows = sample_rows(M, 24, seed=M + N + K)
+        want = O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb, rows=rows)
+        check_bf16(bf16_bits(D)[rows], want, f"{M}x{N}x{K}")
