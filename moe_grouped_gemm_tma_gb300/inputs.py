@@ -21,7 +21,9 @@ cast itself is torch's ``float8_e4m3fn`` conversion (round to nearest even), a l
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass
 
 import numpy as np
 import torch
@@ -29,7 +31,8 @@ import torch
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+_CHUNK = 1 << 21
+_THREADS = max(1, min(16, os.cpu_count() or 1))
 
 E4M3_MAX = 448.0
 SCALE_FLOOR = 1e-4
@@ -61,10 +64,12 @@ def uniforms(seed: int, count: int, start: int = 0) -> np.ndarray:
 
 
 def normals(seed: int, count: int) -> np.ndarray:
-    """``count`` standard normals (float32), Box-Muller over word pairs, generated in chunks."""
+    """``count`` standard normals (float32), Box-Muller over word pairs, generated in chunks (chunks
+    run on a thread pool; numpy releases the GIL, and each chunk's words depend only on its index)."""
     out = np.empty(count, dtype=np.float32)
     pairs = (count + 1) // 2
-    for p0 in range(0, pairs, _CHUNK):
+
+    def chunk(p0):
         npair = min(_CHUNK, pairs - p0)
         u = uniforms(seed, 2 * npair, start=2 * p0).reshape(npair, 2)
         r = np.sqrt(-2.0 * np.log(u[:, 0]))
@@ -73,6 +78,14 @@ def normals(seed: int, count: int) -> np.ndarray:
         lo = 2 * p0
         n = min(2 * npair, count - lo)
         out[lo:lo + n] = z[:n]
+
+    starts = list(range(0, pairs, _CHUNK))
+    if len(starts) <= 1:
+        for p0 in starts:
+            chunk(p0)
+    else:
+        with ThreadPoolExecutor(max_workers=min(len(starts), _THREADS)) as ex:
+            list(ex.map(chunk, starts))
     return out
 
 

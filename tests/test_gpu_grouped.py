@@ -1,0 +1,166 @@
+"""GPU parity of the MoE layouts against the CPU oracle on identical seeded inputs: m-grouped
+contiguous (dg_m_grouped_contiguous), m-grouped masked (dg_m_grouped_masked, with sentinel checks of
+every row past masked_m) and the k-grouped FP32 weight gradient (dg_k_grouped_wgrad)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_tma_gb300 as dg
+from moe_grouped_gemm_tma_gb300 import inputs as I
+from oracle import oracle as O
+from tests.gpu_util import SENTINEL, bf16_bits, check_bf16, check_f32, dev, sample_rows, sentinel_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------------------------------ contiguous
+def run_contiguous(c, m_indices=None):
+    mi = c.m_indices if m_indices is None else m_indices
+    D = sentinel_bf16(c.Mt, c.N)
+    dg.dg_m_grouped_contiguous(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), dev(mi), D)
+    assert dg.dg_device_status() == 0
+    return bf16_bits(D)
+
+
+@pytest.mark.parametrize("G,group_m,N,K", [
+    (3, [130, 0, 77], 256, 256),
+    (4, [128, 1, 255, 300], 2112, 512),
+    (2, [600, 50], 1000, 384),
+])
+def test_contiguous_small_full_parity(G, group_m, N, K):
+    c = I.make_contiguous(I.seed_for(2, sum(group_m)), G, N, K, group_m)
+    got = run_contiguous(c)
+    valid = c.m_indices.numpy() >= 0
+    want = O.m_grouped_contiguous(c.A, c.sfa, c.B, c.sfb, c.m_indices)
+    check_bf16(got[valid], want[valid], f"contiguous G={G}")
+
+
+def test_contiguous_skips_blocks_that_start_with_padding():
+    c = I.make_contiguous(I.seed_for(2, 5), 2, 256, 256, [128, 128])
+    mi = c.m_indices.clone()
+    mi[128:256] = -1   # the second expert's whole block marked as padding
+    got = run_contiguous(c, mi)
+    assert (got[128:256] == SENTINEL).all()
+    want = O.gemm_fp8_nt(c.A[:128], c.sfa[:128], c.B[0], c.sfb[0])
+    check_bf16(got[:128], want, "first block")
+
+
+@pytest.mark.parametrize("G,base,N,K", [(4, 4096, 7168, 2048), (8, 8192, 4096, 7168)])
+def test_contiguous_workload_sampled_rows(G, base, N, K):
+    # the MoE prefill / training-forward workload at full size; rows sampled around every expert boundary
+    sizes = I.contiguous_group_sizes(I.seed_for(2, G), G, base)
+    c = I.make_contiguous(I.seed_for(2, G), G, N, K, sizes)
+    got = run_contiguous(c)
+    mi = c.m_indices.numpy()
+    starts = np.concatenate([[0], np.cumsum([(m + 127) // 128 * 128 for m in sizes])[:-1]])
+    must = [int(s + d) for s, m in zip(starts, sizes) for d in (0, 1, 127, 128, m - 1)]
+    rows = sample_rows(c.Mt, 64, seed=G + base, must=must)
+    rows = rows[mi[rows] >= 0]
+    want = O.m_grouped_contiguous(c.A, c.sfa, c.B, c.sfb, c.m_indices, rows=rows)
+    check_bf16(got[rows], want, f"contiguous G={G} base={base}")
+
+
+# ------------------------------------------------------------------------------------------ masked
+def run_masked(c, masked_m=None, expected_m=0):
+    mm = c.masked_m if masked_m is None else masked_m
+    D = sentinel_bf16(c.G, c.max_m, c.N)
+    dg.dg_m_grouped_masked(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), dev(mm), D, expected_m=expected_m)
+    assert dg.dg_device_status() == 0
+    return bf16_bits(D).reshape(c.G * c.max_m, c.N)
+
+
+def _check_masked(c, got, mm_list, rows=None):
+    valid = np.zeros(c.G * c.max_m, dtype=bool)
+    for g, m in enumerate(mm_list):
+        valid[g * c.max_m: g * c.max_m + min(max(m, 0), c.max_m)] = True
+    assert (got[~valid] == SENTINEL).all(), f"{(got[~valid] != SENTINEL).any(axis=1).sum()} masked rows written"
+    if rows is None:
+        rows = np.nonzero(valid)[0]
+    else:
+        rows = rows[valid[rows]]
+    want = O.m_grouped_masked(c.A, c.sfa, c.B, c.sfb, c.masked_m, rows=rows)
+    check_bf16(got[rows], want, "masked")
+
+
+@pytest.mark.parametrize("G,max_m,masked,N,K", [
+    (3, 256, [10, 0, 256], 256, 256),
+    (4, 192, [129, 128, 127, 1], 2112, 512),
+    (2, 64, [64, 33], 4096, 384),
+])
+def test_masked_small_full_parity_and_untouched_rows(G, max_m, masked, N, K):
+    c = I.make_masked(I.seed_for(3, G * max_m), G, max_m, N, K, masked)
+    got = run_masked(c)
+    _check_masked(c, got, masked)
+
+
+def test_masked_all_empty_and_over_max():
+    c = I.make_masked(I.seed_for(3, 1), 2, 128, 256, 256, [0, 0])
+    got = run_masked(c)
+    assert (got == SENTINEL).all()
+    over = torch.tensor([1000, 3], dtype=torch.int32)
+    c2 = I.MaskedCase(c.G, c.max_m, c.N, c.K, 0, c.A, c.sfa, c.B, c.sfb, over)
+    got = run_masked(c2)
+    _check_masked(c2, got, [128, 3])
+
+
+@pytest.mark.parametrize("bn", [64, 128, 192, 256])
+def test_masked_every_tile_width(bn, monkeypatch):
+    monkeypatch.setenv("DG_BN", str(bn))
+    c = I.make_masked(I.seed_for(3, bn), 3, 256, 1000, 384, [200, 5, 129])
+    _check_masked(c, run_masked(c), [200, 5, 129])
+
+
+@pytest.mark.parametrize("G,max_m,expected_m,N,K", [
+    (16, 256, 64, 4096, 7168), (4, 512, 128, 7168, 2048), (1, 1024, 256, 4096, 7168), (2, 256, 256, 7168, 2048),
+])
+def test_masked_workload_sampled_rows(G, max_m, expected_m, N, K):
+    # the MoE decode workload at full size; every row past masked_m is sentinel-checked
+    sizes = I.masked_sizes(I.seed_for(3, G), G, expected_m, max_m)
+    c = I.make_masked(I.seed_for(3, G), G, max_m, N, K, sizes, expected_m)
+    got = run_masked(c, expected_m=expected_m)
+    must = [g * max_m + d for g, m in enumerate(sizes) for d in (0, m - 1) if m > 0]
+    rows = sample_rows(G * max_m, 48, seed=G * max_m, must=must)
+    _check_masked(c, got, sizes, rows=rows)
+
+
+# ------------------------------------------------------------------------------------------ k-grouped
+def run_kgrouped(c):
+    D = dev(c.D_in)
+    dg.dg_k_grouped_wgrad(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), c.ks, D)
+    assert dg.dg_device_status() == 0
+    return D.cpu().numpy()
+
+
+@pytest.mark.parametrize("ks,M,N", [([256, 0, 384], 200, 264), ([128], 128, 128), ([512, 128, 1024, 256], 300, 1000)])
+def test_kgrouped_small_full_parity(ks, M, N):
+    c = I.make_kgrouped(I.seed_for(4, sum(ks) + M), len(ks), M, N, ks)
+    got = run_kgrouped(c)
+    want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in)
+    for g in range(len(ks)):
+        check_f32(got[g], want[g], f"k-grouped g={g}")
+        if ks[g] == 0:   # an expert with no tokens leaves its gradient buffer bit-for-bit unchanged
+            np.testing.assert_array_equal(got[g], c.D_in[g].numpy())
+
+
+def test_kgrouped_integer_exact_bitwise():
+    rng = np.random.default_rng(9)
+    M, N, ks = 256, 256, [256, 128]
+    vals = np.array([0x00, 0x38, 0x40, 0x44, 0x48, 0xB8, 0xC0, 0xC4, 0xC8], dtype=np.uint8)
+    A = torch.from_numpy(rng.choice(vals, size=(M, sum(ks))))
+    B = torch.from_numpy(rng.choice(vals, size=(N, sum(ks))))
+    sfa, sfb = torch.ones(M, 3), torch.ones(N, 3)
+    D_in = torch.from_numpy(rng.integers(-100, 100, size=(2, M, N)).astype(np.float32))
+    c = I.KGroupedCase(2, M, N, ks, A, sfa, B, sfb, D_in)
+    np.testing.assert_array_equal(run_kgrouped(c), O.k_grouped_wgrad(A, sfa, B, sfb, ks, D_in))
+
+
+@pytest.mark.parametrize("G,M,N", [(4, 7168, 4096), (8, 2048, 7168)])
+def test_kgrouped_workload_sampled_rows(G, M, N):
+    # the MoE weight-gradient workload at full size (token counts per expert around 4096)
+    ks = I.kgrouped_sizes(I.seed_for(4, G), G, 4096)
+    c = I.make_kgrouped(I.seed_for(4, G), G, M, N, ks)
+    got = run_kgrouped(c)
+    rows = sample_rows(M, 16, seed=G + M)
+    want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in, rows=rows)
+    for g in range(G):
+        check_f32(got[g][rows], want[g], f"k-grouped g={g}")
