@@ -86,86 +86,89 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
-// BN candidates per layout; each must have a specialisation in the matching dg_inst_*.cu file.
-constexpr int kBnNormal[] = {64, 96, 128, 160, 192, 224, 256};
-constexpr int kBnContiguous[] = {128, 160, 192, 224, 256};
-constexpr int kBnMasked[] = {64, 128, 192, 256};
-constexpr int kBnKGrouped[] = {128};
+// Specialisations per layout: (BN, PAIR); each must be instantiated in the matching dg_inst_*.cu.
+struct Spec {
+    int bn, pair;
+};
+constexpr Spec kNormalSpecs1[] = {{64, 1}, {96, 1}, {128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
+constexpr Spec kNormalSpecs2[] = {{128, 2}, {160, 2}, {192, 2}, {224, 2}, {256, 2}};
+constexpr Spec kContiguousSpecs[] = {{128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
+constexpr Spec kMaskedSpecs1[] = {{64, 1}, {128, 1}, {192, 1}, {256, 1}};
+constexpr Spec kMaskedSpecs2[] = {{128, 2}, {256, 2}};
+constexpr Spec kKGroupedSpecs1[] = {{128, 1}};
+constexpr Spec kKGroupedSpecs2[] = {{128, 2}};
 
 // Pick BN minimising waves * (BN + per-tile overhead), ties to the larger BN: the time of one wave of
-// 128 x BN tiles grows with BN, and the number of waves is the tile count over the SM count.
+// (128 * PAIR) x BN tiles grows with BN, and the number of waves is the tile count over the number of
+// tiles that run at once (SMs / PAIR).
 template <size_t NC>
-int choose_bn(const int (&cands)[NC], int64_t row_blocks, int n, int sms) {
-    int best = cands[NC - 1];
+Spec choose_spec(const Spec (&cands)[NC], int64_t row_units, int n, int sms) {
+    Spec best = cands[NC - 1];
     int64_t best_cost = INT64_MAX;
     for (size_t i = 0; i < NC; ++i) {
-        const int bn = cands[i];
-        const int64_t tiles = row_blocks * cdiv(n, bn);
-        const int64_t waves = (tiles + sms - 1) / sms;
+        const int bn = cands[i].bn;
+        const int64_t slots = sms / cands[i].pair;
+        const int64_t tiles = row_units * cdiv(n, bn);
+        const int64_t waves = (tiles + slots - 1) / slots;
         const int64_t cost = waves * (bn + 16);
-        if (cost <= best_cost) { best_cost = cost; best = bn; }
+        if (cost <= best_cost) { best_cost = cost; best = cands[i]; }
     }
     return best;
 }
 
-template <int MODE>
-cudaError_t launch_bn(int bn, const Launch& L);
-
-template <>
-cudaError_t launch_bn<kNormal>(int bn, const Launch& L) {
-    switch (bn) {
-        case 64: return launch<kNormal, 64>(L);
-        case 96: return launch<kNormal, 96>(L);
-        case 128: return launch<kNormal, 128>(L);
-        case 160: return launch<kNormal, 160>(L);
-        case 192: return launch<kNormal, 192>(L);
-        case 224: return launch<kNormal, 224>(L);
-        case 256: return launch<kNormal, 256>(L);
-    }
-    return cudaErrorInvalidValue;
-}
-
-template <>
-cudaError_t launch_bn<kContiguous>(int bn, const Launch& L) {
-    switch (bn) {
-        case 128: return launch<kContiguous, 128>(L);
-        case 160: return launch<kContiguous, 160>(L);
-        case 192: return launch<kContiguous, 192>(L);
-        case 224: return launch<kContiguous, 224>(L);
-        case 256: return launch<kContiguous, 256>(L);
-    }
-    return cudaErrorInvalidValue;
-}
-
-template <>
-cudaError_t launch_bn<kMasked>(int bn, const Launch& L) {
-    switch (bn) {
-        case 64: return launch<kMasked, 64>(L);
-        case 128: return launch<kMasked, 128>(L);
-        case 192: return launch<kMasked, 192>(L);
-        case 256: return launch<kMasked, 256>(L);
-    }
-    return cudaErrorInvalidValue;
-}
-
-template <>
-cudaError_t launch_bn<kKGrouped>(int bn, const Launch& L) {
-    switch (bn) {
-        case 128: return launch<kKGrouped, 128>(L);
-    }
-    return cudaErrorInvalidValue;
-}
-
 // Optional override of the tile width, for tuning sweeps only (DG_BN=<n>); ignored unless valid.
 template <size_t NC>
-int bn_override(const int (&cands)[NC], int chosen) {
+Spec spec_override(const Spec (&cands)[NC], Spec chosen) {
     const char* s = getenv("DG_BN");
     if (!s) return chosen;
     const int v = atoi(s);
     for (size_t i = 0; i < NC; ++i)
-        if (cands[i] == v) return v;
+        if (cands[i].bn == v) return cands[i];
     return chosen;
 }
+
+// CTA pairs only pay off when a 256-row tile is mostly real rows; DG_PAIR=1/2 overrides for sweeps.
+bool use_pair(int64_t rows_per_group) {
+    const char* s = getenv("DG_PAIR");
+    if (s) return atoi(s) == 2;
+    return rows_per_group > 128;
+}
+
+template <int MODE>
+cudaError_t launch_spec(Spec sp, const Launch& L);
+
+#define DG_CASE(M, B, P) \
+    if (sp.bn == B && sp.pair == P) return launch<M, B, P>(L);
+
+template <>
+cudaError_t launch_spec<kNormal>(Spec sp, const Launch& L) {
+    DG_CASE(kNormal, 64, 1) DG_CASE(kNormal, 96, 1) DG_CASE(kNormal, 128, 1) DG_CASE(kNormal, 160, 1)
+    DG_CASE(kNormal, 192, 1) DG_CASE(kNormal, 224, 1) DG_CASE(kNormal, 256, 1)
+    DG_CASE(kNormal, 128, 2) DG_CASE(kNormal, 160, 2) DG_CASE(kNormal, 192, 2) DG_CASE(kNormal, 224, 2)
+    DG_CASE(kNormal, 256, 2)
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_spec<kContiguous>(Spec sp, const Launch& L) {
+    DG_CASE(kContiguous, 128, 1) DG_CASE(kContiguous, 160, 1) DG_CASE(kContiguous, 192, 1)
+    DG_CASE(kContiguous, 224, 1) DG_CASE(kContiguous, 256, 1)
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_spec<kMasked>(Spec sp, const Launch& L) {
+    DG_CASE(kMasked, 64, 1) DG_CASE(kMasked, 128, 1) DG_CASE(kMasked, 192, 1) DG_CASE(kMasked, 256, 1)
+    DG_CASE(kMasked, 128, 2) DG_CASE(kMasked, 256, 2)
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_spec<kKGrouped>(Spec sp, const Launch& L) {
+    DG_CASE(kKGrouped, 128, 1) DG_CASE(kKGrouped, 128, 2)
+    return cudaErrorInvalidValue;
+}
+#undef DG_CASE
 
 dg_status common_prologue(DeviceInfo* dev) {
     dg_status st = device_info(dev);
@@ -223,11 +226,14 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
     if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
 
-    const int bn = bn_override(kBnNormal, choose_bn(kBnNormal, cdiv(M, BM), N, dev.sms));
+    const bool pair = use_pair(M);
+    const Spec sp = pair ? spec_override(kNormalSpecs2, choose_spec(kNormalSpecs2, cdiv(M, 2 * BM), N, dev.sms))
+                         : spec_override(kNormalSpecs1, choose_spec(kNormalSpecs1, cdiv(M, BM), N, dev.sms));
+    const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, M, K, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_operand_map(&L.tmap_b, B, N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
     p.sfb = sfb;
@@ -238,14 +244,15 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
     p.kbs = K / 128;
     p.groups = 1;
     p.sfb_rows = cdiv(N, 128);
-    p.m_blocks = cdiv(M, BM);
+    p.m_blocks = cdiv(M, BM * sp.pair);
     p.n_blocks = cdiv(N, bn);
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);
-    L.grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    L.units = p.tiles;
+    L.sms = dev.sms;
     L.stream = stream;
-    return launch_bn<kNormal>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    return launch_spec<kNormal>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
 }
 
 dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
@@ -264,7 +271,8 @@ dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint
     dg_status st = common_prologue(&dev);
     if (st != DG_OK) return st;
 
-    const int bn = bn_override(kBnContiguous, choose_bn(kBnContiguous, cdiv(Mt, BM), N, dev.sms));
+    const Spec sp = spec_override(kContiguousSpecs, choose_spec(kContiguousSpecs, cdiv(Mt, BM), N, dev.sms));
+    const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, Mt, K, BM) != DG_OK) return DG_CUDA_ERROR;
@@ -285,9 +293,10 @@ dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);
-    L.grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    L.units = p.tiles;
+    L.sms = dev.sms;
     L.stream = stream;
-    return launch_bn<kContiguous>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    return launch_spec<kContiguous>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
 }
 
 dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
@@ -308,11 +317,14 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     if (st != DG_OK) return st;
 
     const int hint = (expected_m > 0 && expected_m < max_m) ? expected_m : max_m;
-    const int bn = bn_override(kBnMasked, choose_bn(kBnMasked, static_cast<int64_t>(G) * cdiv(hint, BM), N, dev.sms));
+    const bool pair = use_pair(hint);
+    const Spec sp = pair ? spec_override(kMaskedSpecs2, choose_spec(kMaskedSpecs2, static_cast<int64_t>(G) * cdiv(hint, 2 * BM), N, dev.sms))
+                         : spec_override(kMaskedSpecs1, choose_spec(kMaskedSpecs1, static_cast<int64_t>(G) * cdiv(hint, BM), N, dev.sms));
+    const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, static_cast<int64_t>(G) * max_m, K, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
     p.sfb = sfb;
@@ -324,14 +336,15 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     p.kbs = K / 128;
     p.groups = G;
     p.sfb_rows = cdiv(N, 128);
-    p.m_blocks = cdiv(max_m, BM);
+    p.m_blocks = cdiv(max_m, BM * sp.pair);
     p.n_blocks = cdiv(N, bn);
     const int64_t max_tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
     if (max_tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = 0;  // counted on the device from masked_m
-    L.grid = static_cast<int>(max_tiles < dev.sms ? max_tiles : dev.sms);
+    L.units = static_cast<int>(max_tiles);
+    L.sms = dev.sms;
     L.stream = stream;
-    return launch_bn<kMasked>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    return launch_spec<kMasked>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
 }
 
 dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
@@ -355,11 +368,14 @@ dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* 
     dg_status st = common_prologue(&dev);
     if (st != DG_OK) return st;
 
-    const int bn = bn_override(kBnKGrouped, choose_bn(kBnKGrouped, static_cast<int64_t>(G) * cdiv(M, BM), N, dev.sms));
+    const bool pair = use_pair(M);
+    const Spec sp = pair ? spec_override(kKGroupedSpecs2, choose_spec(kKGroupedSpecs2, static_cast<int64_t>(G) * cdiv(M, 2 * BM), N, dev.sms))
+                         : spec_override(kKGroupedSpecs1, choose_spec(kKGroupedSpecs1, static_cast<int64_t>(G) * cdiv(M, BM), N, dev.sms));
+    const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, M, sumK, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_operand_map(&L.tmap_b, B, N, sumK, bn) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, sumK, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
     p.sfb = sfb;
@@ -370,7 +386,7 @@ dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* 
     p.kbs = static_cast<int>(sumK / 128);
     p.groups = G;
     p.sfb_rows = N;
-    p.m_blocks = cdiv(M, BM);
+    p.m_blocks = cdiv(M, BM * sp.pair);
     p.n_blocks = cdiv(N, bn);
     int off = 0;
     for (int g = 0; g < G; ++g) {
@@ -381,9 +397,10 @@ dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* 
     const int64_t tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);
-    L.grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    L.units = p.tiles;
+    L.sms = dev.sms;
     L.stream = stream;
-    return launch_bn<kKGrouped>(bn, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    return launch_spec<kKGrouped>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
 }
 
 }  // extern "C"

@@ -3,9 +3,9 @@
 #include "dg_launch.cuh"
 
 namespace dg {
-template cudaError_t launch<kContiguous, 128>(const Launch&);
-template cudaError_t launch<kContiguous, 160>(const Launch&);
-template cudaError_t launch<kContiguous, 192>(const Launch&);
-template cudaError_t launch<kContiguous, 224>(const Launch&);
-template cudaError_t launch<kContiguous, 256>(const Launch&);
+template cudaError_t launch<kContiguous, 128, 1>(const Launch&);
+template cudaError_t launch<kContiguous, 160, 1>(const Launch&);
+template cudaError_t launch<kContiguous, 192, 1>(const Launch&);
+template cudaError_t launch<kContiguous, 224, 1>(const Launch&);
+template cudaError_t launch<kContiguous, 256, 1>(const Launch&);
 }  // namespace dg

@@ -3,5 +3,6 @@
 #include "dg_launch.cuh"
 
 namespace dg {
-template cudaError_t launch<kKGrouped, 128>(const Launch&);
+template cudaError_t launch<kKGrouped, 128, 1>(const Launch&);
+template cudaError_t launch<kKGrouped, 128, 2>(const Launch&);
 }  // namespace dg

@@ -3,8 +3,10 @@
 #include "dg_launch.cuh"
 
 namespace dg {
-template cudaError_t launch<kMasked, 64>(const Launch&);
-template cudaError_t launch<kMasked, 128>(const Launch&);
-template cudaError_t launch<kMasked, 192>(const Launch&);
-template cudaError_t launch<kMasked, 256>(const Launch&);
+template cudaError_t launch<kMasked, 64, 1>(const Launch&);
+template cudaError_t launch<kMasked, 128, 1>(const Launch&);
+template cudaError_t launch<kMasked, 192, 1>(const Launch&);
+template cudaError_t launch<kMasked, 256, 1>(const Launch&);
+template cudaError_t launch<kMasked, 128, 2>(const Launch&);
+template cudaError_t launch<kMasked, 256, 2>(const Launch&);
 }  // namespace dg

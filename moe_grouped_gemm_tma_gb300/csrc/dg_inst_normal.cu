@@ -3,11 +3,16 @@
 #include "dg_launch.cuh"
 
 namespace dg {
-template cudaError_t launch<kNormal, 64>(const Launch&);
-template cudaError_t launch<kNormal, 96>(const Launch&);
-template cudaError_t launch<kNormal, 128>(const Launch&);
-template cudaError_t launch<kNormal, 160>(const Launch&);
-template cudaError_t launch<kNormal, 192>(const Launch&);
-template cudaError_t launch<kNormal, 224>(const Launch&);
-template cudaError_t launch<kNormal, 256>(const Launch&);
+template cudaError_t launch<kNormal, 64, 1>(const Launch&);
+template cudaError_t launch<kNormal, 96, 1>(const Launch&);
+template cudaError_t launch<kNormal, 128, 1>(const Launch&);
+template cudaError_t launch<kNormal, 160, 1>(const Launch&);
+template cudaError_t launch<kNormal, 192, 1>(const Launch&);
+template cudaError_t launch<kNormal, 224, 1>(const Launch&);
+template cudaError_t launch<kNormal, 256, 1>(const Launch&);
+template cudaError_t launch<kNormal, 128, 2>(const Launch&);
+template cudaError_t launch<kNormal, 160, 2>(const Launch&);
+template cudaError_t launch<kNormal, 192, 2>(const Launch&);
+template cudaError_t launch<kNormal, 224, 2>(const Launch&);
+template cudaError_t launch<kNormal, 256, 2>(const Launch&);
 }  // namespace dg

@@ -7,17 +7,28 @@
 //
 //   D[m,n] = sum_kb sfa[m,kb] * sfb(n,kb) * P_kb[m,n],   P_kb[m,n] = sum_{k in block kb} A[m,k] B[n,k]
 //
-// One CTA per SM runs a static round-robin over output tiles of 128 x BN. Its warps have fixed roles:
-//   warp 0      TMA producer: one lane streams the A [128 x 128] and B [BN x 128] e4m3 tiles of every
-//               K block into a STAGES-deep shared-memory ring (128-byte swizzle), signalling `full`.
-//   warp 1      TMEM owner and MMA issuer: one lane issues four tcgen05.mma (M=128, N=BN, K=32) per
-//               K block into one of NACC TMEM accumulators, then commits to the stage's `empty`
-//               barrier (smem reusable) and the accumulator's `tmem_full` barrier.
-//   warps 2..9  promotion / epilogue: two warpgroups split the BN columns; each thread owns one tile
-//               row (its TMEM lane) and BN/2 FP32 running sums in registers. Per K block they read the
-//               block partial out of TMEM, multiply by sfa[m,kb] * sfb and add (packed f32x2 FMA), and
-//               release the accumulator (`tmem_empty`). At the end of a tile they round to BF16 (or
-//               add into FP32 for the weight gradient) and store.
+// Output tiles are (128 * PAIR) x BN. With PAIR = 1 one CTA owns a 128-row tile; with PAIR = 2 a
+// cluster of two CTAs on two SMs owns a 256-row tile: each CTA loads its own 128 rows of A and half
+// (BN/2 rows) of B, the leader CTA issues tcgen05.mma.cta_group::2 (M = 256) which reads both CTAs'
+// shared memory and writes each CTA's 128 accumulator rows into that CTA's TMEM. Per SM this halves
+// the B bytes staged per K block.
+//
+// Warp roles (every CTA; 3 warpgroups):
+//   warp 0      TMA producer: one lane streams the A and B tiles of every K block into a STAGES-deep
+//               shared-memory ring (128-byte swizzle). The leader's `full` barrier expects the bytes
+//               of both CTAs; the peer's loads signal it across the pair.
+//   warp 1      TMEM owner (512 columns) and, in the leader, the MMA issuer: one lane issues four
+//               MMAs (K = 32) per K block into one of NACC TMEM accumulators, then commits (to both
+//               CTAs of a pair) the stage's `empty` barrier and the accumulator's `tmem_full` barrier.
+//   warp 2      scale stager: per K block, cp.async copies of the block's sfa column (this CTA's 128
+//               rows) and the sfb values the tile needs into a SCALE_SLOTS-deep shared ring, running
+//               ahead of the epilogue so no scale load latency reaches it.
+//   warps 4..11 promotion / epilogue (two warpgroups, registers raised with setmaxnreg): the
+//               warpgroups split the BN columns; each thread owns one tile row (its TMEM lane) and
+//               BN/2 FP32 running sums. Per K block they read the block partial out of TMEM (64
+//               columns per wait), multiply by sfa[m,kb] * sfb and add (packed f32x2 FMA), and release
+//               the accumulator (`tmem_empty` in the leader) and the scale slot. At the end of a tile
+//               they round to BF16 (or add into FP32 for the weight gradient) and store.
 // The MMA of K block kb+1.. overlaps the promotion of block kb (NACC accumulators in flight), and the
 // store of one tile overlaps the first MMAs of the next.
 //
@@ -33,12 +44,16 @@
 
 namespace dg {
 
-constexpr int BM = 128;                 // tile rows = UMMA M (one TMEM lane per row)
+constexpr int BM = 128;                 // rows per CTA = UMMA M per CTA (one TMEM lane per row)
 constexpr int BK = 128;                 // K block = scaling block
 constexpr int UMMA_K = 32;              // K of one kind::f8f6f4 MMA
+constexpr int EPI_WARP0 = 4;            // first epilogue warp
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int THREADS = 128 + 32 * EPI_WARPS;
+constexpr int CTRL_REGS = 56;           // registers per thread of warpgroup 0 after setmaxnreg
+constexpr int EPI_REGS = 224;           // ... of the epilogue warpgroups (128*56 + 256*224 = 384*168)
 constexpr int TMEM_COLS = 512;
+constexpr int SCALE_SLOTS = 16;
 constexpr int MAX_MASKED_G = 1024;
 constexpr int MAX_KGROUPS = 128;
 constexpr int SMEM_LIMIT = 232448;      // 227 KB per CTA on sm_100-family parts
@@ -60,41 +75,50 @@ struct Params {
     int kbs;                   // K blocks per scale row (K/128, or sumK/128)
     int groups;
     int sfb_rows;              // ceil(N/128), or N for the per-row k-grouped scales
-    int m_blocks;              // ceil(rows / BM)
+    int m_blocks;              // row blocks of (BM * PAIR) rows: ceil(rows / (BM * PAIR))
     int n_blocks;              // ceil(n / BN)
     int tiles;                 // tile count when known on the host (not masked)
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
-template <int MODE, int BN>
+template <int MODE, int BN, int PAIR>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+    static_assert(PAIR == 1 || PAIR == 2, "PAIR is 1 or 2");
+    static constexpr int TILE_M = BM * PAIR;
     static constexpr int A_BYTES = BM * BK;
-    static constexpr int B_BYTES = BN * BK;
+    static constexpr int B_ROWS = BN / PAIR;            // B rows staged by each CTA
+    static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int SFB_BYTES = (MODE == kKGrouped) ? 2 * BN * 4 : 0;
-    static constexpr int STATIC_RESERVE = 512 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - SFB_BYTES - STATIC_RESERVE) / STAGE_BYTES;
+    // scale slot: sfa of the CTA's 128 rows, then sfb: 4 block rows (from n0/128), or BN per-row values
+    static constexpr int SB = (MODE == kKGrouped) ? BN : 4;
+    static constexpr int SLOT_FLOATS = BM + SB;
+    static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
+    static constexpr int STATIC_RESERVE = 1024 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - SCALE_BYTES - STATIC_RESERVE) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int NACC_FIT = TMEM_COLS / BN;
     static constexpr int NACC = NACC_FIT > 4 ? 4 : NACC_FIT;
-    static constexpr int DYN_SMEM = 1024 + STAGES * STAGE_BYTES + SFB_BYTES;
+    static constexpr int DYN_SMEM = 1024 + STAGES * STAGE_BYTES + SCALE_BYTES;
     static constexpr int COLS = BN / 2;        // columns per epilogue warpgroup
     static constexpr int CHUNKS = COLS / 16;   // 16-column TMEM loads per K block
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
+    static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte swizzle-atom alignment");
 };
 
 struct TileInfo {
-    int g, m0, n0;
+    int g, m0, n0;       // m0: first row of this CTA's 128-row part (within the expert for masked)
     int kb0, nkb;        // K blocks [kb0, kb0 + nkb)
-    int a_row, b_row;    // TMA row coordinates of the first A / B row
-    int d_row;           // output row of the tile's first row
-    int rows_valid;      // rows of the tile that are stored
+    int a_row, b_row;    // TMA row coordinates of this CTA's first A / B row
+    int d_row;           // output row of this CTA's first row
+    int rows_valid;      // rows of this CTA's part that are stored (may be <= 0)
     bool valid;
 };
 
-template <int MODE, int BN>
-__device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const int* s_prefix) {
+template <int MODE, int BN, int PAIR>
+__device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const int* s_prefix, int rank) {
+    constexpr int TILE_M = BM * PAIR;
+    constexpr int B_ROWS = BN / PAIR;
     TileInfo ti;
     ti.valid = true;
     ti.g = 0;
@@ -102,17 +126,17 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
     ti.nkb = p.kbs;
     if (MODE == kNormal || MODE == kContiguous) {
         const int mb = t % p.m_blocks, nb = t / p.m_blocks;
-        ti.m0 = mb * BM;
+        ti.m0 = mb * TILE_M + rank * BM;
         ti.n0 = nb * BN;
         ti.a_row = ti.m0;
         ti.d_row = ti.m0;
         ti.rows_valid = min(BM, p.rows - ti.m0);
-        ti.b_row = ti.n0;
+        ti.b_row = ti.n0 + rank * B_ROWS;
         if (MODE == kContiguous) {
-            const int g = __ldg(p.m_indices + ti.m0);
+            const int g = __ldg(p.m_indices + mb * TILE_M);
             ti.valid = (g >= 0 && g < p.groups);
             ti.g = ti.valid ? g : 0;
-            ti.b_row = ti.g * p.n + ti.n0;
+            ti.b_row += ti.g * p.n;
         }
     } else if (MODE == kMasked) {
         // s_prefix[g] = tiles of experts < g; find the expert whose tile range holds t
@@ -127,24 +151,24 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
         const int mb = local % mblk, nb = local / mblk;
         const int mm = min(max(__ldg(p.masked_m + g), 0), p.rows);
         ti.g = g;
-        ti.m0 = mb * BM;
+        ti.m0 = mb * TILE_M + rank * BM;
         ti.n0 = nb * BN;
         ti.a_row = g * p.rows + ti.m0;
         ti.d_row = ti.a_row;
-        ti.b_row = g * p.n + ti.n0;
+        ti.b_row = g * p.n + ti.n0 + rank * B_ROWS;
         ti.rows_valid = min(BM, mm - ti.m0);
     } else {  // kKGrouped
         const int per_g = p.m_blocks * p.n_blocks;
         const int g = t / per_g, local = t - g * per_g;
         const int mb = local % p.m_blocks, nb = local / p.m_blocks;
         ti.g = g;
-        ti.m0 = mb * BM;
+        ti.m0 = mb * TILE_M + rank * BM;
         ti.n0 = nb * BN;
         ti.kb0 = p.kb_off[g];
         ti.nkb = p.kb_off[g + 1] - p.kb_off[g];
         ti.valid = ti.nkb > 0;
         ti.a_row = ti.m0;
-        ti.b_row = ti.n0;
+        ti.b_row = ti.n0 + rank * B_ROWS;
         ti.d_row = g * p.rows + ti.m0;
         ti.rows_valid = min(BM, p.rows - ti.m0);
     }
@@ -170,7 +194,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
     }
 }
 
-// Short bounded wait used only while draining after an abort.
+// Short bounded wait used only while draining.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -182,33 +206,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int MODE, int BN>
+__device__ __forceinline__ float pick4(const float4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+template <int MODE, int BN, int PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ Params p) {
-    using C = Cfg<MODE, BN>;
+    using C = Cfg<MODE, BN, PAIR>;
     constexpr int STAGES = C::STAGES;
     constexpr int NACC = C::NACC;
     constexpr int COLS = C::COLS;
     constexpr int CHUNKS = C::CHUNKS;
-    constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+    constexpr uint32_t IDESC = idesc_e4m3_f32(C::TILE_M, BN);
 
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ uint64_t tmem_full_bar[NACC], tmem_empty_bar[NACC];
+    __shared__ uint64_t scale_full_bar[SCALE_SLOTS], scale_empty_bar[SCALE_SLOTS];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_prefix[MODE == kMasked ? MAX_MASKED_G + 1 : 1];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = (PAIR == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+    const bool leader = (rank == 0);
+    const int unit = (PAIR == 2) ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+    const int num_units = (PAIR == 2) ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
-    // 1024-byte aligned operand ring (128-byte swizzle atoms are 1024 bytes)
+    // 1024-byte aligned operand ring (128-byte swizzle atoms are 1024 bytes); identical offsets in
+    // both CTAs of a pair, which the pair MMA relies on
     const uint32_t raw = smem_u32(dyn_smem);
     uint8_t* smem = dyn_smem + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + STAGES * C::A_BYTES;
-    float* s_sfb = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+    float* s_scales = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -217,20 +251,29 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(&tmem_full_bar[a], 1);
-            mbar_init(&tmem_empty_bar[a], EPI_WARPS);
+            mbar_init(&tmem_empty_bar[a], EPI_WARPS * PAIR);
+        }
+        for (int s = 0; s < SCALE_SLOTS; ++s) {
+            mbar_init(&scale_full_bar[s], 32);
+            mbar_init(&scale_empty_bar[s], EPI_WARPS);
         }
         s_abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&s_tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR == 2) {
+            tmem_alloc_pair(&s_tmem_base, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&s_tmem_base, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (MODE == kMasked) {
         // per-expert tile counts, then an exclusive prefix sum (one warp)
         for (int g = threadIdx.x; g < p.groups; g += THREADS) {
             const int mm = min(max(__ldg(p.masked_m + g), 0), p.rows);
-            s_prefix[g + 1] = ((mm + BM - 1) / BM) * p.n_blocks;
+            s_prefix[g + 1] = ((mm + C::TILE_M - 1) / C::TILE_M) * p.n_blocks;
         }
         __syncthreads();
         if (warp == 0) {
@@ -250,53 +293,67 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = s_tmem_base;
     volatile int* abort_flag = &s_abort;
     const int num_tiles = (MODE == kMasked) ? s_prefix[p.groups] : p.tiles;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp < EPI_WARP0) {
+        regs_dec<CTRL_REGS>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------------ TMA producer
             prefetch_tmap(&tmap_a);
             prefetch_tmap(&tmap_b);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;   // per-stage bits, for the abort drain
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<MODE, BN>(p, t, s_prefix);
+            for (int t = unit; t < num_tiles && ok; t += num_units) {
+                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
                     const int x = (ti.kb0 + kb) * BK;
-                    tma_load_2d(&tmap_a, &full_bar[stage], smem_a + stage * C::A_BYTES, x, ti.a_row);
-                    tma_load_2d(&tmap_b, &full_bar[stage], smem_b + stage * C::B_BYTES, x, ti.b_row);
+                    uint8_t* a_dst = smem_a + stage * C::A_BYTES;
+                    uint8_t* b_dst = smem_b + stage * C::B_BYTES;
+                    if (PAIR == 1 || leader) {
+                        mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
+                        tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
+                        tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                    } else {
+                        const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                        tma_load_2d_pair(&tmap_a, bar, a_dst, x, ti.a_row);
+                        tma_load_2d_pair(&tmap_b, bar, b_dst, x, ti.b_row);
+                    }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (!ok) {
+            if (ok) {
+                // wait until every stage this CTA filled has been consumed, so no MMA-completion
+                // arrival can still be in flight towards this CTA when it exits
+                for (int i = 0; i < STAGES && ok; ++i) {
+                    if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) ok = false;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok && (PAIR == 1 || leader)) {
                 for (int s = 0; s < STAGES; ++s)
                     if (issued & (1u << s)) drain_wait(&full_bar[s], (issued_parity >> s) & 1u);
             }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0 && leader) {
+            // ------------------------------------------------------------------ MMA issuer
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
             int last_acc = 0;
             uint32_t last_parity = 0;
             const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<MODE, BN>(p, t, s_prefix);
+            for (int t = unit; t < num_tiles && ok; t += num_units) {
+                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -306,11 +363,19 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     const uint32_t a_addr = a_base + stage * C::A_BYTES;
                     const uint32_t b_addr = b_base + stage * C::B_BYTES;
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k)
-                        mma_f8f6f4(d_tmem, sw128_kmajor_desc(a_addr + k * UMMA_K),
-                                   sw128_kmajor_desc(b_addr + k * UMMA_K), IDESC, k > 0 ? 1u : 0u);
-                    mma_commit(&empty_bar[stage]);
-                    mma_commit(&tmem_full_bar[acc]);
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        const uint64_t ad = sw128_kmajor_desc(a_addr + k * UMMA_K);
+                        const uint64_t bd = sw128_kmajor_desc(b_addr + k * UMMA_K);
+                        if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                        else mma_f8f6f4(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                    }
+                    if (PAIR == 2) {
+                        mma_commit_pair(&empty_bar[stage], 0x3);
+                        mma_commit_pair(&tmem_full_bar[acc], 0x3);
+                    } else {
+                        mma_commit(&empty_bar[stage]);
+                        mma_commit(&tmem_full_bar[acc]);
+                    }
                     any = true;
                     last_acc = acc;
                     last_parity = acc_phase;
@@ -319,26 +384,65 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 }
             }
             if (!ok && any) drain_wait(&tmem_full_bar[last_acc], last_parity);
+        } else if (warp == 2) {
+            // ------------------------------------------------------------------ scale stager
+            int slot = 0;
+            uint32_t sphase = 0;
+            const int a_rows_total = (MODE == kMasked) ? p.groups * p.rows : p.rows;
+            for (int t = unit; t < num_tiles; t += num_units) {
+                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
+                if (!ti.valid) continue;
+                const float* sfa_rows[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    sfa_rows[i] = p.sfa + static_cast<size_t>(min(ti.a_row + lane + 32 * i, a_rows_total - 1)) * p.kbs + ti.kb0;
+                const float* sfb_src;
+                if (MODE == kKGrouped) {
+                    sfb_src = p.sfb + ti.kb0;   // row n: + n * kbs
+                } else {
+                    const int blk = min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1);
+                    sfb_src = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + blk) * p.kbs + ti.kb0;
+                }
+                bool ok = true;
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    float* dst = s_scales + slot * C::SLOT_FLOATS;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + kb);
+                    if (MODE == kKGrouped) {
+                        for (int j = lane; j < BN; j += 32)
+                            cp_async_4(dst + BM + j, sfb_src + static_cast<size_t>(min(ti.n0 + j, p.n - 1)) * p.kbs + kb);
+                    } else if (lane < 4) {
+                        cp_async_4(dst + BM + lane, sfb_src + kb);
+                    }
+                    cp_async_arrive_noinc(&scale_full_bar[slot]);
+                    if (++slot == SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            cp_async_wait_all();
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ promotion + epilogue
-        const int ew = warp - 2;               // 0..7
+        regs_inc<EPI_REGS>();
+        const int ew = warp - EPI_WARP0;       // 0..7
         const int q = warp & 3;                // TMEM lane quarter this warp may access
         const int h = ew >> 2;                 // column half of the tile
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * COLS;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        uint32_t it = 0;                       // K blocks processed so far (scale-slot parity)
+        int acc = 0, slot = 0;
+        uint32_t acc_phase = 0, sphase = 0;
         bool ok = true;
 
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const TileInfo ti = decode_tile<MODE, BN>(p, t, s_prefix);
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+            const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
             if (!ti.valid) continue;
             const int cstart = ti.n0 + h * COLS;   // first output column of this thread
-            const int arow = min(ti.a_row + row_in_tile, (MODE == kMasked ? p.groups * p.rows : p.rows) - 1);
-            const float* sfa_row = p.sfa + static_cast<size_t>(arow) * p.kbs + ti.kb0;
+            // sfb block rows of this thread's columns, as indices into the slot's 4 staged rows
+            const int bidx = cstart / 128 - ti.n0 / 128;
+            const int split = (128 * (cstart / 128 + 1) - cstart) / 16;   // chunks before the next block
 
             float accum[COLS];
             if (MODE == kKGrouped) {
@@ -356,69 +460,43 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 for (int j = 0; j < COLS; ++j) accum[j] = 0.f;
             }
 
-            // sfb rows that this thread's columns fall into
-            const float* sfb_g = p.sfb + static_cast<size_t>(ti.g) * p.sfb_rows * p.kbs + ti.kb0;
-            const int bblk = cstart / 128;
-            const int split = (128 * (bblk + 1) - cstart) / 16;     // chunks before the next 128-block
-            const float* sfb0 = sfb_g + static_cast<size_t>(min(bblk, p.sfb_rows - 1)) * p.kbs;
-            const float* sfb1 = sfb_g + static_cast<size_t>(min(bblk + 1, p.sfb_rows - 1)) * p.kbs;
-            // k-grouped: this thread stages one per-column scale per K block
-            const int my_col = cstart + (threadIdx.x & 127);
-            const bool stage_col = (MODE == kKGrouped) && ((threadIdx.x & 127) < COLS) && my_col < p.n;
-            const float* sfb_col = p.sfb + static_cast<size_t>(stage_col ? my_col : 0) * p.kbs + ti.kb0;
-
-            float sa_next = __ldg(sfa_row);
-            float sb0_next = (MODE == kKGrouped) ? 0.f : __ldg(sfb0);
-            float sb1_next = (MODE == kKGrouped) ? 0.f : __ldg(sfb1);
-            float sc_next = stage_col ? __ldg(sfb_col) : 0.f;
-
             for (int kb = 0; kb < ti.nkb; ++kb) {
-                const float sa = sa_next, sb0 = sb0_next, sb1 = sb1_next, sc = sc_next;
-                if (kb + 1 < ti.nkb) {           // prefetch the next K block's scales
-                    sa_next = __ldg(sfa_row + kb + 1);
-                    if (MODE != kKGrouped) {
-                        sb0_next = __ldg(sfb0 + kb + 1);
-                        sb1_next = __ldg(sfb1 + kb + 1);
-                    } else if (stage_col) {
-                        sc_next = __ldg(sfb_col + kb + 1);
-                    }
-                }
-                // k-grouped: publish this K block's per-column scales to the warpgroup; the slot
-                // alternates on a running counter, so a slot is rewritten only after every thread
-                // of the warpgroup has passed the barrier of the block that last used it
-                float* slot = s_sfb + (it & 1) * BN + h * COLS;
-                ++it;
-                if (MODE == kKGrouped && (threadIdx.x & 127) < COLS) slot[threadIdx.x & 127] = sc;
-
-                const bool got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status);
-                // abort decisions are uniform per warp (and per warpgroup when it shares a barrier)
-                const bool all_ok = (MODE == kKGrouped) ? named_bar_and(1 + h, 128, got)
-                                                        : __all_sync(0xffffffffu, got);
-                if (!all_ok) { ok = false; break; }
+                const bool got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
+                                 wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = lane_addr + static_cast<uint32_t>(acc * BN);
+                const float* sl = s_scales + slot * C::SLOT_FLOATS;
+                const float sa = sl[row_in_tile];
+                float s0 = 0.f, s1 = 0.f;
+                if (MODE != kKGrouped) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
+                    s0 = sa * pick4(b4, bidx);
+                    s1 = sa * pick4(b4, bidx + 1 < 4 ? bidx + 1 : 3);
+                }
+                const float* scol = sl + BM + h * COLS;   // k-grouped per-column scales
 
 #pragma unroll
-                for (int c0 = 0; c0 < CHUNKS; c0 += 2) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld_x16(taddr + c0 * 16, r0);
-                    if (c0 + 1 < CHUNKS) tmem_ld_x16(taddr + (c0 + 1) * 16, r1);
+                for (int c0 = 0; c0 < CHUNKS; c0 += 4) {
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        if (c0 + cc < CHUNKS) tmem_ld_x16(taddr + (c0 + cc) * 16, r[cc]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
+                    for (int cc = 0; cc < 4; ++cc) {
                         const int c = c0 + cc;
                         if (c >= CHUNKS) break;
-                        const uint32_t* r = cc ? r1 : r0;
                         if (MODE == kKGrouped) {
                             const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
                             for (int j = 0; j < 16; j += 4) {
-                                const float4 sv = *reinterpret_cast<const float4*>(slot + c * 16 + j);
+                                const float4 sv = *reinterpret_cast<const float4*>(scol + c * 16 + j);
                                 float2 a0 = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
                                 float2 a1 = make_float2(accum[c * 16 + j + 2], accum[c * 16 + j + 3]);
-                                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[cc][j]), __uint_as_float(r[cc][j + 1])),
                                                              make_float2(sv.x, sv.y));
-                                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[cc][j + 2]), __uint_as_float(r[cc][j + 3])),
                                                              make_float2(sv.z, sv.w));
                                 a0 = __ffma2_rn(p0, sa2, a0);
                                 a1 = __ffma2_rn(p1, sa2, a1);
@@ -426,12 +504,12 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                                 accum[c * 16 + j + 2] = a1.x; accum[c * 16 + j + 3] = a1.y;
                             }
                         } else {
-                            const float s = sa * ((c < split) ? sb0 : sb1);
+                            const float s = (c < split) ? s0 : s1;
                             const float2 s2 = make_float2(s, s);
 #pragma unroll
                             for (int j = 0; j < 16; j += 2) {
                                 float2 a = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
-                                a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2, a);
+                                a = __ffma2_rn(make_float2(__uint_as_float(r[cc][j]), __uint_as_float(r[cc][j + 1])), s2, a);
                                 accum[c * 16 + j] = a.x;
                                 accum[c * 16 + j + 1] = a.y;
                             }
@@ -440,12 +518,18 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tmem_empty_bar[acc]);
+                if (lane == 0) {
+                    // the accumulator is released on the leader's barrier (the peer's is unused)
+                    if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
+                    else mbar_arrive(&tmem_empty_bar[acc]);
+                    mbar_arrive(&scale_empty_bar[slot]);
+                }
                 if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
+                if (++slot == SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
             }
             if (!ok) break;
 
-            // ---- store the tile
+            // ---- store this CTA's rows of the tile
             if (row_in_tile < ti.rows_valid) {
                 if (MODE == kKGrouped) {
                     float* drow = reinterpret_cast<float*>(p.d) + static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
@@ -469,10 +553,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 
     // ---------------------------------------------------------------------- teardown
     tc_fence_before();
-    __syncthreads();
+    if (PAIR == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

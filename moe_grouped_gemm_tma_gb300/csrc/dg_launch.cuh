@@ -1,5 +1,5 @@
-// Host-side launch of one kernel specialisation (mode, BN). Each dg_inst_*.cu file instantiates the
-// specialisations of one mode, so the kernels compile in parallel translation units.
+// Host-side launch of one kernel specialisation (mode, BN, CTA pair). Each dg_inst_*.cu file
+// instantiates the specialisations of one mode, so the kernels compile in parallel translation units.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -12,32 +12,54 @@ struct Launch {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;
     Params params;
-    int grid;
+    int units;          // work units wanted: tiles (single CTA) or tile pairs (CTA pairs)
+    int sms;
     cudaStream_t stream;
 };
 
-template <int MODE, int BN>
+template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L);
 
-template <int MODE, int BN>
-int dyn_smem_bytes() { return Cfg<MODE, BN>::DYN_SMEM; }
-
 #ifdef DG_DEFINE_LAUNCH
-template <int MODE, int BN>
+template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L) {
-    using C = Cfg<MODE, BN>;
-    auto kern = dg_gemm_kernel<MODE, BN>;
-    // the attribute is per function and cheap to set; setting it every call keeps this free of
-    // per-device caches
+    using C = Cfg<MODE, BN, PAIR>;
+    auto kern = dg_gemm_kernel<MODE, BN, PAIR>;
+    // the attribute is per function and cheap to set
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
     if (e != cudaSuccess) return e;
+    // the warpgroups re-split the launch's registers with setmaxnreg; that split must equal what the
+    // kernel was compiled to launch with, or a raising warpgroup would wait forever
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * THREADS != CTRL_REGS * 128 + EPI_REGS * (THREADS - 128)) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
+    cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::DYN_SMEM;
     cfg.stream = L.stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    if (PAIR == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // persistent: as many pairs as can be resident at once (one CTA per SM)
+        cfg.gridDim = dim3(2u * static_cast<unsigned>(L.sms / 2), 1, 1);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
+            clusters = L.sms / 2;
+        const int units = L.units < clusters ? L.units : clusters;
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
+    } else {
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        const int units = L.units < L.sms ? L.units : L.sms;
+        cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+    }
+    if (cfg.gridDim.x == 0) return cudaSuccess;
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.params);
 }
 #endif

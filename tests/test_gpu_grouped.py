@@ -103,11 +103,12 @@ def test_masked_all_empty_and_over_max():
     _check_masked(c2, got, [128, 3])
 
 
-@pytest.mark.parametrize("bn", [64, 128, 192, 256])
-def test_masked_every_tile_width(bn, monkeypatch):
+@pytest.mark.parametrize("bn,pair", [(64, 1), (128, 1), (192, 1), (256, 1), (128, 2), (256, 2)])
+def test_masked_every_tile_shape(bn, pair, monkeypatch):
     monkeypatch.setenv("DG_BN", str(bn))
-    c = I.make_masked(I.seed_for(3, bn), 3, 256, 1000, 384, [200, 5, 129])
-    _check_masked(c, run_masked(c), [200, 5, 129])
+    monkeypatch.setenv("DG_PAIR", str(pair))
+    c = I.make_masked(I.seed_for(3, bn), 3, 384, 1000, 384, [300, 5, 129])
+    _check_masked(c, run_masked(c), [300, 5, 129])
 
 
 @pytest.mark.parametrize("G,max_m,expected_m,N,K", [
@@ -131,8 +132,10 @@ def run_kgrouped(c):
     return D.cpu().numpy()
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("ks,M,N", [([256, 0, 384], 200, 264), ([128], 128, 128), ([512, 128, 1024, 256], 300, 1000)])
-def test_kgrouped_small_full_parity(ks, M, N):
+def test_kgrouped_small_full_parity(ks, M, N, pair, monkeypatch):
+    monkeypatch.setenv("DG_PAIR", str(pair))
     c = I.make_kgrouped(I.seed_for(4, sum(ks) + M), len(ks), M, N, ks)
     got = run_kgrouped(c)
     want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in)

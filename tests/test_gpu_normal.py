@@ -37,13 +37,19 @@ def test_normal_shapes_full_parity(M, N, K):
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"{M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("bn", [64, 96, 128, 160, 192, 224, 256])
-def test_every_tile_width(bn, monkeypatch):
-    # ragged in M (two row blocks, the second partial) and in N for every BN
+SPECS = [(bn, 1) for bn in (64, 96, 128, 160, 192, 224, 256)] + [(bn, 2) for bn in (128, 160, 192, 224, 256)]
+
+
+@pytest.mark.parametrize("bn,pair", SPECS)
+@pytest.mark.parametrize("M", [200, 520])
+def test_every_tile_shape(bn, pair, M, monkeypatch):
+    # ragged in M (the last row block partial; for CTA pairs also a pair whose second CTA has no rows)
+    # and in N, for every tile width, single-CTA and CTA-pair tiles
     monkeypatch.setenv("DG_BN", str(bn))
-    c = I.make_normal(I.seed_for(1, 900 + bn), 200, 1000, 512)
+    monkeypatch.setenv("DG_PAIR", str(pair))
+    c = I.make_normal(I.seed_for(1, 900 + bn + M), M, 1000, 512)
     D = run_normal(c)
-    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn}")
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn} pair={pair}")
 
 
 def test_integer_exact_bitwise():
