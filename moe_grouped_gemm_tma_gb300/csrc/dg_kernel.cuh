@@ -302,10 +302,14 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 
     if (warp < EPI_WARP0) {
         regs_dec<CTRL_REGS>();
-        if (warp == 0 && lane == 0) {
+        if (warp == 0) {
             // ------------------------------------------------------------------ TMA producer
-            prefetch_tmap(&tmap_a);
-            prefetch_tmap(&tmap_b);
+            // The whole warp runs the loop (warp-uniform operands); one elected lane issues.
+            const bool issuer = elect_one();
+            if (issuer) {
+                prefetch_tmap(&tmap_a);
+                prefetch_tmap(&tmap_b);
+            }
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;   // per-stage bits, for the abort drain
@@ -314,19 +318,25 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const int x = (ti.kb0 + kb) * BK;
                     uint8_t* a_dst = smem_a + stage * C::A_BYTES;
                     uint8_t* b_dst = smem_b + stage * C::B_BYTES;
                     if (PAIR == 1 || leader) {
-                        mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
-                        tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
-                        tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                        if (issuer) {
+                            mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
+                            tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
+                            tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                        }
                     } else {
                         const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
-                        tma_load_2d_pair(&tmap_a, bar, a_dst, x, ti.a_row);
-                        tma_load_2d_pair(&tmap_b, bar, b_dst, x, ti.b_row);
+                        if (issuer) {
+                            tma_load_2d_pair(&tmap_a, bar, a_dst, x, ti.a_row);
+                            tma_load_2d_pair(&tmap_b, bar, b_dst, x, ti.b_row);
+                        }
                     }
+                    __syncwarp();
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -336,16 +346,20 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 // wait until every stage this CTA filled has been consumed, so no MMA-completion
                 // arrival can still be in flight towards this CTA when it exits
                 for (int i = 0; i < STAGES && ok; ++i) {
-                    if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) ok = false;
+                    const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, got)) ok = false;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (!ok && (PAIR == 1 || leader)) {
+            if (!ok && (PAIR == 1 || leader) && issuer) {
                 for (int s = 0; s < STAGES; ++s)
                     if (issued & (1u << s)) drain_wait(&full_bar[s], (issued_parity >> s) & 1u);
             }
-        } else if (warp == 1 && lane == 0 && leader) {
+        } else if (warp == 1 && leader) {
             // ------------------------------------------------------------------ MMA issuer
+            // The whole warp runs the loop so descriptors and TMEM addresses are warp-uniform (kept in
+            // uniform registers); one elected lane issues the MMAs and commits.
+            const bool issuer = elect_one();
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
@@ -356,26 +370,32 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    if (!wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    if (!wait_bounded(&full_bar[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                    const bool got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status) &&
+                                     wait_bounded(&full_bar[stage], phase, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                    const uint32_t a_addr = a_base + stage * C::A_BYTES;
-                    const uint32_t b_addr = b_base + stage * C::B_BYTES;
+                    const uint64_t a_desc = sw128_kmajor_desc(a_base + stage * C::A_BYTES);
+                    const uint64_t b_desc = sw128_kmajor_desc(b_base + stage * C::B_BYTES);
+                    if (issuer) {
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
-                        const uint64_t ad = sw128_kmajor_desc(a_addr + k * UMMA_K);
-                        const uint64_t bd = sw128_kmajor_desc(b_addr + k * UMMA_K);
-                        if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
-                        else mma_f8f6f4(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            // advancing the start address by 32 bytes (>> 4 = 2) steps K by 32 within
+                            // the 128-byte swizzle row
+                            const uint64_t ad = a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
+                            const uint64_t bd = b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
+                            if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                            else mma_f8f6f4(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                        }
+                        if (PAIR == 2) {
+                            mma_commit_pair(&empty_bar[stage], 0x3);
+                            mma_commit_pair(&tmem_full_bar[acc], 0x3);
+                        } else {
+                            mma_commit(&empty_bar[stage]);
+                            mma_commit(&tmem_full_bar[acc]);
+                        }
                     }
-                    if (PAIR == 2) {
-                        mma_commit_pair(&empty_bar[stage], 0x3);
-                        mma_commit_pair(&tmem_full_bar[acc], 0x3);
-                    } else {
-                        mma_commit(&empty_bar[stage]);
-                        mma_commit(&tmem_full_bar[acc]);
-                    }
+                    __syncwarp();
                     any = true;
                     last_acc = acc;
                     last_parity = acc_phase;
@@ -383,7 +403,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
                 }
             }
-            if (!ok && any) drain_wait(&tmem_full_bar[last_acc], last_parity);
+            if (!ok && any && issuer) drain_wait(&tmem_full_bar[last_acc], last_parity);
         } else if (warp == 2) {
             // ------------------------------------------------------------------ scale stager
             int slot = 0;
@@ -476,17 +496,35 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 }
                 const float* scol = sl + BM + h * COLS;   // k-grouped per-column scales
 
+                // Loads and promotion are software-pipelined over groups of 32 columns (two x16 loads)
+                // in two alternating register buffers: group g+1's TMEM loads are in flight while group g
+                // is promoted. The accumulator is released right after its last load has completed,
+                // before the last group's FMAs; the scale slot after the FMAs that read it.
+                constexpr int NG = (CHUNKS + 1) / 2;
+                uint32_t rb[2][2][16];
+                tmem_ld_x16(taddr, rb[0][0]);
+                if (CHUNKS > 1) tmem_ld_x16(taddr + 16, rb[0][1]);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c0 = 0; c0 < CHUNKS; c0 += 4) {
-                    uint32_t r[4][16];
+                for (int g = 0; g < NG; ++g) {
+                    const int b = g & 1;
+                    if (g + 1 < NG) {
+                        tmem_ld_x16(taddr + (g + 1) * 32, rb[b ^ 1][0]);
+                        if (2 * (g + 1) + 1 < CHUNKS) tmem_ld_x16(taddr + (g + 1) * 32 + 16, rb[b ^ 1][1]);
+                    } else {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // the accumulator is released on the leader's barrier (the peer's is unused)
+                            if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
+                            else mbar_arrive(&tmem_empty_bar[acc]);
+                        }
+                    }
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        if (c0 + cc < CHUNKS) tmem_ld_x16(taddr + (c0 + cc) * 16, r[cc]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int c = c0 + cc;
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * g + cc;
                         if (c >= CHUNKS) break;
+                        const uint32_t* r = rb[b][cc];
                         if (MODE == kKGrouped) {
                             const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
@@ -494,9 +532,9 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                                 const float4 sv = *reinterpret_cast<const float4*>(scol + c * 16 + j);
                                 float2 a0 = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
                                 float2 a1 = make_float2(accum[c * 16 + j + 2], accum[c * 16 + j + 3]);
-                                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[cc][j]), __uint_as_float(r[cc][j + 1])),
+                                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
                                                              make_float2(sv.x, sv.y));
-                                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[cc][j + 2]), __uint_as_float(r[cc][j + 3])),
+                                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
                                                              make_float2(sv.z, sv.w));
                                 a0 = __ffma2_rn(p0, sa2, a0);
                                 a1 = __ffma2_rn(p1, sa2, a1);
@@ -509,21 +547,17 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 #pragma unroll
                             for (int j = 0; j < 16; j += 2) {
                                 float2 a = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
-                                a = __ffma2_rn(make_float2(__uint_as_float(r[cc][j]), __uint_as_float(r[cc][j + 1])), s2, a);
+                                a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2, a);
                                 accum[c * 16 + j] = a.x;
                                 accum[c * 16 + j + 1] = a.y;
                             }
                         }
                     }
+                    if (g + 1 < NG) tmem_ld_wait();
                 }
-                tc_fence_before();
+                // every lane has read its scales (the FMAs above used them)
                 __syncwarp();
-                if (lane == 0) {
-                    // the accumulator is released on the leader's barrier (the peer's is unused)
-                    if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
-                    else mbar_arrive(&tmem_empty_bar[acc]);
-                    mbar_arrive(&scale_empty_bar[slot]);
-                }
+                if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
                 if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
                 if (++slot == SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
             }
