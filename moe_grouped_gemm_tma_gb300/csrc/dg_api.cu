@@ -82,6 +82,19 @@ dg_status make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int64
     return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
 }
 
+// Row-major BF16 output [rows, n] written in boxes of 32 rows x 16 columns (32 bytes) with the
+// 32-byte swizzle the epilogue's staging buffers use.
+dg_status make_output_map(CUtensorMap* m, void* base, int64_t rows, int64_t n) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(n) * 2};
+    cuuint32_t box[2] = {16u, 32u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
@@ -127,11 +140,41 @@ Spec spec_override(const Spec (&cands)[NC], Spec chosen) {
     return chosen;
 }
 
-// CTA pairs only pay off when a 256-row tile is mostly real rows; DG_PAIR=1/2 overrides for sweeps.
+// Split-K for problems whose tiles cannot fill half the SMs (small M): a cluster of S CTAs shares a
+// tile, each CTA streaming K/S of it, so more SMs pull operands at once. Picks (BN, S) with the most
+// CTAs that still fit in one wave, at least 4 K blocks per CTA; ties go to the smaller S. DG_SPLIT=<s>
+// forces S (1 disables) for sweeps.
+template <size_t NC>
+int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, int kbs, int sms) {
+    const char* env = getenv("DG_SPLIT");
+    if (env) {
+        const int s = atoi(env);
+        return (s == 2 || s == 4 || s == 8) && kbs >= s ? s : 1;
+    }
+    if (getenv("DG_BN")) return 1;
+    if (row_blocks * cdiv(n, sp->bn) * 2 > sms) return 1;
+    int best_split = 1;
+    int64_t best_ctas = row_blocks * cdiv(n, sp->bn);
+    for (int s = 2; s <= 8; s *= 2) {
+        if (kbs < 4 * s) break;
+        for (size_t i = 0; i < NC; ++i) {
+            const int64_t ctas = row_blocks * cdiv(n, cands[i].bn) * s;
+            if (ctas <= sms && ctas > best_ctas) {
+                best_ctas = ctas;
+                best_split = s;
+                *sp = cands[i];
+            }
+        }
+    }
+    return best_split;
+}
+
+// CTA-pair (256-row) tiles halve the per-SM B traffic, but with the promotion epilogue as the limit
+// they currently lose to single-CTA tiles on every measured shape (the cross-SM accumulator handoff
+// lengthens the MMA/promotion loop), so they are opt-in: DG_PAIR=2 (only for more than 128 rows).
 bool use_pair(int64_t rows_per_group) {
     const char* s = getenv("DG_PAIR");
-    if (s) return atoi(s) == 2;
-    return rows_per_group > 128;
+    return s && atoi(s) == 2 && rows_per_group > 128;
 }
 
 template <int MODE>
@@ -227,13 +270,15 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
 
     const bool pair = use_pair(M);
-    const Spec sp = pair ? spec_override(kNormalSpecs2, choose_spec(kNormalSpecs2, cdiv(M, 2 * BM), N, dev.sms))
-                         : spec_override(kNormalSpecs1, choose_spec(kNormalSpecs1, cdiv(M, BM), N, dev.sms));
+    Spec sp = pair ? spec_override(kNormalSpecs2, choose_spec(kNormalSpecs2, cdiv(M, 2 * BM), N, dev.sms))
+                   : spec_override(kNormalSpecs1, choose_spec(kNormalSpecs1, cdiv(M, BM), N, dev.sms));
+    const int split = pair ? 1 : choose_split(kNormalSpecs1, &sp, cdiv(M, BM), N, K / 128, dev.sms);
     const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, M, K, BM) != DG_OK) return DG_CUDA_ERROR;
     if (make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
+    if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
     p.sfb = sfb;
@@ -246,6 +291,7 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
     p.sfb_rows = cdiv(N, 128);
     p.m_blocks = cdiv(M, BM * sp.pair);
     p.n_blocks = cdiv(N, bn);
+    p.split = split;
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);
@@ -276,6 +322,7 @@ dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, Mt, K, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_output_map(&L.tmap_d, D, Mt, N) != DG_OK) return DG_CUDA_ERROR;
     if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
@@ -324,6 +371,7 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, static_cast<int64_t>(G) * max_m, K, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_output_map(&L.tmap_d, D, static_cast<int64_t>(G) * max_m, N) != DG_OK) return DG_CUDA_ERROR;
     if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;

@@ -78,6 +78,7 @@ struct Params {
     int m_blocks;              // row blocks of (BM * PAIR) rows: ceil(rows / (BM * PAIR))
     int n_blocks;              // ceil(n / BN)
     int tiles;                 // tile count when known on the host (not masked)
+    int split;                 // normal layout, single-CTA tiles: CTAs (a cluster) sharing one tile's K
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
@@ -94,14 +95,23 @@ struct Cfg {
     static constexpr int SB = (MODE == kKGrouped) ? BN : 4;
     static constexpr int SLOT_FLOATS = BM + SB;
     static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
+    // output staging for TMA stores: per epilogue warp two 1 KB boxes of 32 rows x 16 BF16 columns
+    static constexpr bool TMA_STORE = (MODE != kKGrouped);
+    static constexpr int STORE_BYTES = TMA_STORE ? EPI_WARPS * 2048 : 0;
     static constexpr int STATIC_RESERVE = 1024 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - SCALE_BYTES - STATIC_RESERVE) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - SCALE_BYTES - 1024 - STORE_BYTES - STATIC_RESERVE) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static constexpr int NACC_FIT = TMEM_COLS / BN;
-    static constexpr int NACC = NACC_FIT > 4 ? 4 : NACC_FIT;
-    static constexpr int DYN_SMEM = 1024 + STAGES * STAGE_BYTES + SCALE_BYTES;
+    static constexpr int NACC = NACC_FIT > 8 ? 8 : NACC_FIT;
+    static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + SCALE_BYTES + 1023) / 1024) * 1024;
+    static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
     static constexpr int COLS = BN / 2;        // columns per epilogue warpgroup
     static constexpr int CHUNKS = COLS / 16;   // 16-column TMEM loads per K block
+    // split-K partial sums: [128 rows][BN + 4] FP32 (padded rows: conflict-free 16-byte stores), in the
+    // operand ring, which is idle once the tile's last MMA has completed
+    static constexpr int PSTRIDE = BN + 4;
+    static constexpr int PARTIAL_BYTES = BM * PSTRIDE * 4;
+    static_assert(PARTIAL_BYTES <= STAGES * STAGE_BYTES, "split-K partials must fit in the operand ring");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte swizzle-atom alignment");
 };
@@ -116,7 +126,7 @@ struct TileInfo {
 };
 
 template <int MODE, int BN, int PAIR>
-__device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const int* s_prefix, int rank) {
+__device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const int* s_prefix, int rank, int srank) {
     constexpr int TILE_M = BM * PAIR;
     constexpr int B_ROWS = BN / PAIR;
     TileInfo ti;
@@ -132,6 +142,10 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
         ti.d_row = ti.m0;
         ti.rows_valid = min(BM, p.rows - ti.m0);
         ti.b_row = ti.n0 + rank * B_ROWS;
+        if (MODE == kNormal && p.split > 1) {   // this CTA's share of the tile's K blocks
+            ti.kb0 = (srank * p.kbs) / p.split;
+            ti.nkb = ((srank + 1) * p.kbs) / p.split - ti.kb0;
+        }
         if (MODE == kContiguous) {
             const int g = __ldg(p.m_indices + mb * TILE_M);
             ti.valid = (g >= 0 && g < p.groups);
@@ -213,7 +227,7 @@ __device__ __forceinline__ float pick4(const float4& v, int i) {
 template <int MODE, int BN, int PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-               const __grid_constant__ Params p) {
+               const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ Params p) {
     using C = Cfg<MODE, BN, PAIR>;
     constexpr int STAGES = C::STAGES;
     constexpr int NACC = C::NACC;
@@ -231,10 +245,15 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int rank = (PAIR == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+    // split-K: a cluster of p.split CTAs shares one tile (one tile per cluster), each CTA a K range
+    const bool split_k = (MODE == kNormal && PAIR == 1 && p.split > 1);
+    const int crank = (PAIR == 2 || split_k) ? static_cast<int>(cluster_ctarank()) : 0;
+    const int rank = (PAIR == 2) ? crank : 0;      // row half of a CTA-pair tile
+    const int srank = split_k ? crank : 0;         // K share of a split-K tile
     const bool leader = (rank == 0);
-    const int unit = (PAIR == 2) ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
-    const int num_units = (PAIR == 2) ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+    const int csize = (PAIR == 2) ? 2 : (split_k ? p.split : 1);
+    const int unit = static_cast<int>(blockIdx.x) / csize;
+    const int num_units = static_cast<int>(gridDim.x) / csize;
 
     // 1024-byte aligned operand ring (128-byte swizzle atoms are 1024 bytes); identical offsets in
     // both CTAs of a pair, which the pair MMA relies on
@@ -243,6 +262,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + STAGES * C::A_BYTES;
     float* s_scales = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+    uint8_t* s_store = smem + C::STORE_OFF;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -315,7 +335,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             uint32_t issued = 0, issued_parity = 0;   // per-stage bits, for the abort drain
             bool ok = true;
             for (int t = unit; t < num_tiles && ok; t += num_units) {
-                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
+                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
@@ -367,7 +387,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             uint32_t last_parity = 0;
             const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
             for (int t = unit; t < num_tiles && ok; t += num_units) {
-                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
+                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     const bool got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status) &&
@@ -410,7 +430,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             uint32_t sphase = 0;
             const int a_rows_total = (MODE == kMasked) ? p.groups * p.rows : p.rows;
             for (int t = unit; t < num_tiles; t += num_units) {
-                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
+                const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
                 const float* sfa_rows[4];
 #pragma unroll
@@ -454,10 +474,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * COLS;
         int acc = 0, slot = 0;
         uint32_t acc_phase = 0, sphase = 0;
+        uint32_t store_round = 0;              // TMA-store boxes issued so far (staging half parity)
         bool ok = true;
 
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank);
+            const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
             if (!ti.valid) continue;
             const int cstart = ti.n0 + h * COLS;   // first output column of this thread
             // sfb block rows of this thread's columns, as indices into the slot's 4 staged rows
@@ -563,8 +584,42 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             }
             if (!ok) break;
 
+            if (split_k) {
+                // ---- split-K: park this CTA's FP32 partial sums in shared memory for the reduction
+                float* prow = reinterpret_cast<float*>(smem) + row_in_tile * C::PSTRIDE + h * COLS;
+#pragma unroll
+                for (int j = 0; j < COLS; j += 4)
+                    *reinterpret_cast<float4*>(prow + j) = make_float4(accum[j], accum[j + 1], accum[j + 2], accum[j + 3]);
+                continue;
+            }
             // ---- store this CTA's rows of the tile
-            if (row_in_tile < ti.rows_valid) {
+            if (C::TMA_STORE && (MODE != kMasked || ti.rows_valid >= BM)) {
+                // Stage 32 rows x 16 columns per round in one of the warp's two 1 KB halves (32-byte
+                // swizzle: a row's two 16-byte chunks swap places every 4 rows, so the warp's stores
+                // hit all banks), then one lane issues the TMA store of the box; TMA clips rows and
+                // columns outside D. A half is rewritten only after its previous box has been read.
+                uint8_t* wbuf = s_store + ew * 2048;
+                const int y = ti.d_row + q * 32;
+                const int sw = (lane >> 2) & 1;
+#pragma unroll
+                for (int c = 0; c < CHUNKS; ++c) {
+                    uint8_t* half = wbuf + (store_round & 1u) * 1024;
+                    ++store_round;
+                    if (lane == 0) bulk_wait_read_1();
+                    __syncwarp();
+                    uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
+                    rowp[sw] = make_uint4(pack_bf16x2(accum[c * 16 + 0], accum[c * 16 + 1]), pack_bf16x2(accum[c * 16 + 2], accum[c * 16 + 3]),
+                                          pack_bf16x2(accum[c * 16 + 4], accum[c * 16 + 5]), pack_bf16x2(accum[c * 16 + 6], accum[c * 16 + 7]));
+                    rowp[sw ^ 1] = make_uint4(pack_bf16x2(accum[c * 16 + 8], accum[c * 16 + 9]), pack_bf16x2(accum[c * 16 + 10], accum[c * 16 + 11]),
+                                              pack_bf16x2(accum[c * 16 + 12], accum[c * 16 + 13]), pack_bf16x2(accum[c * 16 + 14], accum[c * 16 + 15]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_d, half, cstart + c * 16, y);
+                        bulk_commit();
+                    }
+                }
+            } else if (row_in_tile < ti.rows_valid) {
                 if (MODE == kKGrouped) {
                     float* drow = reinterpret_cast<float*>(p.d) + static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
 #pragma unroll
@@ -583,6 +638,40 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 }
             }
         }
+        // every TMA store of this warp has completed (and released its staging buffer) before exit
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------------- split-K reduction
+    if (split_k) {
+        // every CTA's partials are visible cluster-wide after this barrier; CTA s of the cluster then
+        // reduces rows [s*128/S, (s+1)*128/S) of the tile over all S partials (fixed order s = 0..S-1),
+        // rounds to BF16 and stores; the second barrier keeps every CTA's shared memory alive until
+        // all remote reads are done
+        cluster_sync();
+        if (warp >= EPI_WARP0 && !*abort_flag) {
+            const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, unit, s_prefix, rank, srank);
+            const int rows_per = BM / p.split;
+            const int groups = rows_per * (BN / 4);
+            const uint32_t part_local = smem_u32(smem);
+            for (int gi = static_cast<int>(threadIdx.x) - EPI_WARP0 * 32; gi < groups; gi += EPI_WARPS * 32) {
+                const int row = srank * rows_per + gi / (BN / 4);
+                const int c4 = (gi % (BN / 4)) * 4;
+                const uint32_t off = static_cast<uint32_t>((row * C::PSTRIDE + c4) * 4);
+                float4 sum = ld_shared_cluster_v4(mapa_shared(part_local + off, 0));
+                for (int sidx = 1; sidx < p.split; ++sidx) {
+                    const float4 v = ld_shared_cluster_v4(mapa_shared(part_local + off, sidx));
+                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                }
+                if (row < ti.rows_valid && ti.n0 + c4 < p.n) {
+                    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) +
+                                         static_cast<size_t>(ti.d_row + row) * p.n + ti.n0 + c4;
+                    st_global_v2(dst, pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+                }
+            }
+        }
+        cluster_sync();
     }
 
     // ---------------------------------------------------------------------- teardown

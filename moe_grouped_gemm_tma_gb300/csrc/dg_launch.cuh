@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "dg_kernel.cuh"
 
 namespace dg {
@@ -11,6 +13,7 @@ namespace dg {
 struct Launch {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;
+    CUtensorMap tmap_d;     // BF16 output boxes for TMA stores (unused by the FP32 k-grouped layout)
     Params params;
     int units;          // work units wanted: tiles (single CTA) or tile pairs (CTA pairs)
     int sms;
@@ -25,21 +28,61 @@ template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L) {
     using C = Cfg<MODE, BN, PAIR>;
     auto kern = dg_gemm_kernel<MODE, BN, PAIR>;
-    // the attribute is per function and cheap to set
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+    // One-time set-up per device for this specialisation (the shared-memory attribute and the checks
+    // below are per function and device; caching them keeps the per-call host cost low).
+    static std::mutex mu;
+    static int ready[64] = {0};
+    static int pair_clusters[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    // the warpgroups re-split the launch's registers with setmaxnreg; that split must equal what the
-    // kernel was compiled to launch with, or a raising warpgroup would wait forever
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs * THREADS != CTRL_REGS * 128 + EPI_REGS * (THREADS - 128)) return cudaErrorInvalidConfiguration;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ready[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+            if (e != cudaSuccess) return e;
+            // the warpgroups re-split the launch's registers with setmaxnreg; that split must equal what
+            // the kernel was compiled to launch with, or a raising warpgroup would wait forever
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, kern);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs * THREADS != CTRL_REGS * 128 + EPI_REGS * (THREADS - 128)) return cudaErrorInvalidConfiguration;
+            if (PAIR == 2) {
+                cudaLaunchConfig_t q = {};
+                cudaLaunchAttribute qa[1];
+                qa[0].id = cudaLaunchAttributeClusterDimension;
+                qa[0].val.clusterDim.x = 2;
+                qa[0].val.clusterDim.y = 1;
+                qa[0].val.clusterDim.z = 1;
+                q.attrs = qa;
+                q.numAttrs = 1;
+                q.blockDim = dim3(THREADS, 1, 1);
+                q.dynamicSmemBytes = C::DYN_SMEM;
+                q.gridDim = dim3(2u * static_cast<unsigned>(L.sms / 2), 1, 1);
+                int clusters = 0;
+                if (cudaOccupancyMaxActiveClusters(&clusters, kern, &q) != cudaSuccess || clusters <= 0)
+                    clusters = L.sms / 2;
+                pair_clusters[dev] = clusters;
+            }
+            ready[dev] = 1;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::DYN_SMEM;
     cfg.stream = L.stream;
-    if (PAIR == 2) {
+    if (MODE == kNormal && PAIR == 1 && L.params.split > 1) {
+        // split-K: one cluster of `split` CTAs per tile, not persistent
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(L.params.split);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(L.units * L.params.split), 1, 1);
+    } else if (PAIR == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -47,10 +90,7 @@ cudaError_t launch(const Launch& L) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         // persistent: as many pairs as can be resident at once (one CTA per SM)
-        cfg.gridDim = dim3(2u * static_cast<unsigned>(L.sms / 2), 1, 1);
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
-            clusters = L.sms / 2;
+        const int clusters = pair_clusters[dev];
         const int units = L.units < clusters ? L.units : clusters;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
     } else {
@@ -60,7 +100,7 @@ cudaError_t launch(const Launch& L) {
         cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
     }
     if (cfg.gridDim.x == 0) return cudaSuccess;
-    return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.params);
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.tmap_d, L.params);
 }
 #endif
 

@@ -52,6 +52,17 @@ def test_every_tile_shape(bn, pair, M, monkeypatch):
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn} pair={pair}")
 
 
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("M,N,K", [(64, 1000, 4096), (128, 2112, 1024), (100, 512, 3200)])
+def test_split_k(split, M, N, K, monkeypatch):
+    # a cluster of `split` CTAs shares each tile's K blocks (unevenly when they do not divide) and
+    # reduces the partial sums through distributed shared memory
+    monkeypatch.setenv("DG_SPLIT", str(split))
+    c = I.make_normal(I.seed_for(1, 700 + split + M + N), M, N, K)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"split={split}")
+
+
 def test_integer_exact_bitwise():
     # unit scales and values in {-1, 0, 1}: every output is an integer <= 256, exact in BF16
     rng = np.random.default_rng(5)
