@@ -240,20 +240,18 @@ def run_ours(args):
     spin_cycles = int(min(2.0, 1.5 * enqueue_s + 0.005) * 2.1e9)
 
     n = len(bufs)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index)
     time.sleep(0.3)
+    # timed region: K steps back to back, only a start and a stop event (events between launches would
+    # serialise them and hide the overlap of one GEMM's set-up with the previous one's tail)
     torch.cuda._sleep(spin_cycles)
     start.record(stream)
-    for s in range(args.steps):
-        ev[s][0].record(stream)
-        for i, b in enumerate(bufs):
-            dg.dg_gemm_fp8_nt(b["A"], b["sfa"], b["B"], b["sfb"], b["D"], stream=stream)
-            ev[s][i + 1].record(stream)
+    for _ in range(args.steps):
+        step()
     stop.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -267,7 +265,19 @@ def run_ours(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
 
-    per_launch = np.array([[ev[s][i].elapsed_time(ev[s][i + 1]) for i in range(n)] for s in range(args.steps)])
+    # per-launch breakdown (roofline of the dominant kernel): a second pass with an event after every
+    # launch, also behind a spin kernel
+    prof_steps = max(1, min(args.steps, 20))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(prof_steps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(min(2.0, 1.5 * (min(host_s) if host_s else 0.01) * (prof_steps + 1) + 0.005) * 2.1e9))
+    for s_ in range(prof_steps):
+        ev[s_][0].record(stream)
+        for i, b in enumerate(bufs):
+            dg.dg_gemm_fp8_nt(b["A"], b["sfa"], b["B"], b["sfb"], b["D"], stream=stream)
+            ev[s_][i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_launch = np.array([[ev[s_][i].elapsed_time(ev[s_][i + 1]) for i in range(n)] for s_ in range(prof_steps)])
     avg_ms = per_launch.mean(axis=0)
     step_flops = sum(flops(*b["shape"]) for b in bufs)
     value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
@@ -346,7 +356,8 @@ def run_ours(args):
                        "l2": "inputs larger than L2: each GEMM has its own buffers, ~1.5 GB per step in all",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "timing": "device time: CUDA events around the K steps, enqueued behind a GPU spin "
-                                 "kernel so host launch cost is excluded (e2e includes it)"},
+                                 "kernel so host launch cost is excluded (e2e includes it); per_shape and "
+                                 "roofline from a second pass with an event after every launch"},
             "roofline": roofline,
             "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": f"first {CPU_SAMPLE_ROWS} rows of each of the 18 GEMMs "

@@ -141,9 +141,9 @@ Spec spec_override(const Spec (&cands)[NC], Spec chosen) {
 }
 
 // Split-K for problems whose tiles cannot fill half the SMs (small M): a cluster of S CTAs shares a
-// tile, each CTA streaming K/S of it, so more SMs pull operands at once. Picks (BN, S) with the most
-// CTAs that still fit in one wave, at least 4 K blocks per CTA; ties go to the smaller S. DG_SPLIT=<s>
-// forces S (1 disables) for sweeps.
+// tile, each CTA streaming K/S of it, so more SMs pull operands at once. Picks (BN, S in {2, 4}) with
+// the most CTAs that still fit in one wave, at least 4 K blocks per CTA; ties go to the smaller S.
+// DG_SPLIT=<s> forces S (2, 4 or 8; 1 disables) for sweeps.
 template <size_t NC>
 int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, int kbs, int sms) {
     const char* env = getenv("DG_SPLIT");
@@ -155,7 +155,7 @@ int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, i
     if (row_blocks * cdiv(n, sp->bn) * 2 > sms) return 1;
     int best_split = 1;
     int64_t best_ctas = row_blocks * cdiv(n, sp->bn);
-    for (int s = 2; s <= 8; s *= 2) {
+    for (int s = 2; s <= 4; s *= 2) {   // clusters of 8 do not all fit at once with one CTA per SM
         if (kbs < 4 * s) break;
         for (size_t i = 0; i < NC; ++i) {
             const int64_t ctas = row_blocks * cdiv(n, cands[i].bn) * s;

@@ -289,6 +289,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             tmem_relinquish();
         }
     }
+    // Everything above touches only shared memory, TMEM and kernel parameters; from here on global
+    // memory is read or written, so wait for the previous grid in the stream (programmatic dependent
+    // launch), and let the next one start its own set-up.
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (MODE == kMasked) {
         // per-expert tile counts, then an exclusive prefix sum (one warp)
         for (int g = threadIdx.x; g < p.groups; g += THREADS) {

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "dg_kernel.cuh"
@@ -22,6 +23,15 @@ struct Launch {
 
 template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L);
+
+// Programmatic dependent launch is on unless DG_PDL=0.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char* s = getenv("DG_PDL");
+        return !(s && s[0] == '0');
+    }();
+    return on;
+}
 
 #ifdef DG_DEFINE_LAUNCH
 template <int MODE, int BN, int PAIR>
@@ -69,7 +79,7 @@ cudaError_t launch(const Launch& L) {
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::DYN_SMEM;
     cfg.stream = L.stream;
@@ -100,6 +110,14 @@ cudaError_t launch(const Launch& L) {
         cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
     }
     if (cfg.gridDim.x == 0) return cudaSuccess;
+    // programmatic dependent launch: the kernel waits (griddepcontrol.wait) before its first global
+    // memory access, so its set-up may overlap the tail of the previous grid in the stream
+    if (pdl_enabled()) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs += 1;
+    }
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.tmap_d, L.params);
 }
 #endif

@@ -297,6 +297,15 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// ------------------------------------------------------------------------------------ PDL
+// Wait until the grids this one depends on (launched before it in the stream) have completed and their
+// memory writes are visible; a no-op when the launch carries no programmatic dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next dependent grid in the stream to be scheduled (its own wait still orders its memory
+// accesses after this grid's completion).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------------ registers
 template <int N>
 __device__ __forceinline__ void regs_dec() {
