@@ -1,21 +1,33 @@
 #!/usr/bin/env python
-"""Throughput of the block-scaled FP8 GEMM on the dense workload, printed as one JSON line.
+"""Throughput of the block-scaled FP8 GEMM and its MoE variants, printed as one JSON line.
 
-Workload (one "step"): the dense normal FP8 GEMM NT, D[M,N] = A[M,K] . B[N,K]^T with 1x128 / 128x128
-FP32 block scales and BF16 output, for every M in {64, 128, 4096} and (N, K) in {(2112, 7168),
-(24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048)}: 18 GEMMs, each on its own
-device buffers (about 1.5 GB in all, far above the 129 MB L2, so no GEMM finds its inputs cached from
-its previous run). Inputs are seeded synthetic N(0,1) values block-quantised to e4m3.
+Workloads (--workload; one "step" = every case of the workload once, each on its own device buffers):
 
-value: FP8 TFLOP/s over the whole step (sum of 2MNK / device time of the step), summed over ranks.
-e2e:   the same through the public API with host buffers: pinned host -> device copies of every GEMM's
+* dense (default): the normal FP8 GEMM NT, D[M,N] = A[M,K] . B[N,K]^T, 1x128 / 128x128 FP32 block
+  scales, BF16 out, for M in {64, 128, 4096} x (N, K) in {(2112, 7168), (24576, 1536), (32768, 512),
+  (7168, 16384), (4096, 7168), (7168, 2048)}: 18 GEMMs, about 1.5 GB of buffers in all.
+* contiguous: m-grouped contiguous layout, G in {4, 8} experts, rows per expert U[0.7, 1.3] x {8192,
+  4096} padded to 128, (N, K) in {(4096, 7168), (7168, 2048)}.
+* masked: m-grouped masked layout (decode), G in {1, 2, 4, 16}, (max_m, expected_m) in {(256, 64),
+  (512, 128), (1024, 256)}, masked_m U[0.7, 1.0] x expected_m, (N, K) as above.
+* kgrouped: k-grouped FP32 weight gradient, G in {4, 8}, tokens per expert U[0.5, 1.5] x 4096 padded
+  to 128, (M, N) in {(7168, 4096), (2048, 7168)}.
+
+Inputs are seeded synthetic N(0,1) values block-quantised to e4m3 (drawn on the GPU with the same
+counter-based generator the tests use on the CPU). Every case has its own buffers, so the working set of
+a step is far above the 129 MB L2 and no case finds its inputs cached from its previous run.
+
+value: TFLOP/s over the whole step (2MNK per case, real rows only), summed over ranks; device time of K
+       steps between a start and a stop event, enqueued behind a GPU spin kernel so host launch cost
+       is excluded.
+e2e:   the same through the public API with host buffers: pinned host -> device copies of every case's
        inputs, the call, and the device -> host copy of every output inside the timed region.
-roofline: the kernel with the largest share of the step, against the measured tensor (FP8 = 2 x the
-       measured BF16 rate) or HBM peak, whichever bounds that shape.
-cpu_baseline / --impl reference: the CPU oracle on a bounded row sample of the same 18 GEMMs.
+roofline: the case with the largest share of the step, against the measured tensor peak (FP8 = 2 x the
+       measured sustained BF16 rate) or HBM peak, whichever bounds it (per_case lists all cases).
+cpu_baseline / --impl reference: the CPU oracle on a bounded row sample of the same cases.
 
-Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]; for N > 1 under
-torch.distributed.run, one replica per rank (the GEMMs are independent; there is no exchange).
+Launch: python bench.py [--gpus N --steps K --warmup W] [--workload W] [--impl reference]; for N > 1
+under torch.distributed.run, one replica per rank (the GEMMs are independent; there is no exchange).
 """
 from __future__ import annotations
 
@@ -37,37 +49,27 @@ if ROOT not in sys.path:
 METRIC = "FP8 GEMM TFLOP/s per shape on 1 GB300; fraction of min(FP8 peak, HBM roofline)"
 MS = (64, 128, 4096)
 NKS = ((2112, 7168), (24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048))
-SHAPES = [(M, N, K) for (N, K) in NKS for M in MS]
-WORKLOAD = ("dense normal FP8 GEMM NT (e4m3, 1x128 / 128x128 FP32 scales, BF16 out), "
-            "M in {64,128,4096} x (N,K) in {(2112,7168),(24576,1536),(32768,512),(7168,16384),(4096,7168),(7168,2048)}")
+WORKLOADS = {
+    "dense": ("dense normal FP8 GEMM NT (e4m3, 1x128 / 128x128 FP32 scales, BF16 out), M in {64,128,4096} x "
+              "(N,K) in {(2112,7168),(24576,1536),(32768,512),(7168,16384),(4096,7168),(7168,2048)}"),
+    "contiguous": ("m-grouped contiguous FP8 GEMM (MoE prefill / training forward), G in {4,8}, rows per expert "
+                   "U[0.7,1.3] x {8192,4096} padded to 128, (N,K) in {(4096,7168),(7168,2048)}, BF16 out"),
+    "masked": ("m-grouped masked FP8 GEMM (MoE decode), G in {1,2,4,16}, (max_m, expected_m) in {(256,64),"
+               "(512,128),(1024,256)}, masked_m U[0.7,1.0] x expected_m, (N,K) in {(4096,7168),(7168,2048)}"),
+    "kgrouped": ("k-grouped FP8 weight-gradient GEMM, FP32 accumulated, G in {4,8}, tokens per expert "
+                 "U[0.5,1.5] x 4096 padded to 128, (M,N) in {(7168,4096),(2048,7168)}"),
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-CPU_SAMPLE_ROWS = 64      # cpu_baseline: rows per GEMM
-REF_SAMPLE_ROWS = 16      # --impl reference: rows per GEMM per step
-
-
-def flops(M, N, K):
-    return 2.0 * M * N * K
-
-
-def algo_bytes(M, N, K):
-    kb, nb = K // 128, (N + 127) // 128
-    return M * K + N * K + 4 * M * kb + 4 * nb * kb + 2 * M * N
+CPU_SAMPLE_ROWS = 64      # cpu_baseline: rows per case
+REF_SAMPLE_ROWS = 16      # --impl reference: rows per case per step
 
 
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
-            p = json.load(f)
-        return p, "measured"
+            return json.load(f), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
-
-
-def roofline_time(M, N, K, peaks):
-    fp8 = 2.0 * peaks["bf16_tflops_sustained"] * 1e12
-    bw = peaks["hbm_gbs"] * 1e9
-    tf, tb = flops(M, N, K) / fp8, algo_bytes(M, N, K) / bw
-    return max(tf, tb), ("tensor" if tf >= tb else "hbm")
 
 
 def kernel_source_digest():
@@ -80,7 +82,7 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(shape):
+def ncu_traffic(name):
     """DRAM bytes per launch from the committed ncu record, if it was taken on the current kernels."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -89,7 +91,7 @@ def ncu_traffic(shape):
         rec = json.load(f)
     if rec.get("kernel_source_digest") != kernel_source_digest():
         return None
-    return rec.get("per_launch_bytes", {}).get("x".join(map(str, shape)))
+    return rec.get("per_launch_bytes", {}).get(name)
 
 
 class ClockSampler:
@@ -104,7 +106,7 @@ class ClockSampler:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
             self.proc = subprocess.Popen(["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -145,49 +147,153 @@ def dist_env():
     return world, rank, local
 
 
-def make_inputs():
-    """Host inputs per (N, K): A for the largest M (smaller M take its first rows) and B, with scales."""
+# ------------------------------------------------------------------------------------------------ cases
+class Case:
+    """One GEMM of a workload: its inputs (on the generation device), work counts and calls."""
+
+    def __init__(self, name, flops, nbytes, inputs, out_shape, out_dtype, call, oracle, init_out=None):
+        self.name, self.flops, self.bytes = name, float(flops), float(nbytes)
+        self.inputs = inputs              # ordered dict name -> tensor (copied H2D in e2e)
+        self.out_shape, self.out_dtype = out_shape, out_dtype
+        self.call = call                  # call(dev_inputs, dev_out, stream)
+        self.oracle = oracle              # oracle(cpu_inputs, rows) -> sampled flops
+        self.init_out = init_out          # output buffer contents that the call accumulates into
+
+
+def dense_cases(only=None):
+    import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
-    need = {}
-    for (M, N, K) in SHAPES:
-        need[(N, K)] = max(need.get((N, K), 0), M)
-    return {(N, K): I.make_normal(I.seed_for(1, 0), M, N, K) for (N, K), M in need.items()}
-
-
-def cpu_oracle_rate(host, rows_per_gemm):
-    """Oracle TFLOP/s on the first `rows_per_gemm` rows of each of the 18 GEMMs, all host threads."""
     from oracle import oracle as O
+    shapes = [(M, N, K) for (N, K) in NKS for M in MS] if only is None else [only]
+    need = {}
+    for (M, N, K) in shapes:
+        need[(N, K)] = max(need.get((N, K), 0), M)
+    big = {(N, K): I.make_normal(I.seed_for(1, 0), M, N, K) for (N, K), M in need.items()}
+    cases = []
+    for (M, N, K) in shapes:
+        c = big[(N, K)]
+        kb, nb = K // 128, (N + 127) // 128
+        inp = {"A": c.A[:M].contiguous(), "sfa": c.sfa[:M].contiguous(), "B": c.B, "sfb": c.sfb}
+        cases.append(Case(
+            f"{M}x{N}x{K}", 2.0 * M * N * K, M * K + N * K + 4 * M * kb + 4 * nb * kb + 2 * M * N, inp, (M, N),
+            torch.bfloat16,
+            lambda d, o, s: dg.dg_gemm_fp8_nt(d["A"], d["sfa"], d["B"], d["sfb"], o, stream=s),
+            lambda h, r: (O.gemm_fp8_nt(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"]), 2.0 * r * h["B"].shape[0] * h["B"].shape[1])[1]))
+    return cases
+
+
+def contiguous_cases():
+    import moe_grouped_gemm_tma_gb300 as dg
+    from moe_grouped_gemm_tma_gb300 import inputs as I
+    from oracle import oracle as O
+    cases = []
+    for (N, K) in ((4096, 7168), (7168, 2048)):
+        for G, base in ((4, 8192), (8, 4096)):
+            seed = I.seed_for(2, G * 10 + base // 4096 + N)
+            sizes = I.contiguous_group_sizes(seed, G, base)
+            c = I.make_contiguous(seed, G, N, K, sizes)
+            rows = sum(sizes)
+            kb, nb = K // 128, (N + 127) // 128
+            inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb, "m_indices": c.m_indices}
+            cases.append(Case(
+                f"G{G}x{rows}rows N{N} K{K}", 2.0 * rows * N * K,
+                rows * K + G * N * K + 4 * rows * kb + 4 * G * nb * kb + 2 * rows * N + 4 * c.Mt, inp, (c.Mt, N),
+                torch.bfloat16,
+                lambda d, o, s: dg.dg_m_grouped_contiguous(d["A"], d["sfa"], d["B"], d["sfb"], d["m_indices"], o, stream=s),
+                lambda h, r: (O.m_grouped_contiguous(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], h["m_indices"][:r]),
+                              2.0 * int((h["m_indices"][:r] >= 0).sum()) * h["B"].shape[1] * h["B"].shape[2])[1]))
+    return cases
+
+
+def masked_cases():
+    import moe_grouped_gemm_tma_gb300 as dg
+    from moe_grouped_gemm_tma_gb300 import inputs as I
+    from oracle import oracle as O
+    cases = []
+    for (N, K) in ((4096, 7168), (7168, 2048)):
+        for G in (1, 2, 4, 16):
+            for max_m, em in ((256, 64), (512, 128), (1024, 256)):
+                seed = I.seed_for(3, G * 1000 + max_m + em + N)
+                sizes = I.masked_sizes(seed, G, em, max_m)
+                c = I.make_masked(seed, G, max_m, N, K, sizes, em)
+                rows = sum(sizes)
+                kb, nb = K // 128, (N + 127) // 128
+                inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb, "masked_m": c.masked_m}
+                cases.append(Case(
+                    f"G{G} max_m{max_m} E[m]{em} rows{rows} N{N} K{K}", 2.0 * rows * N * K,
+                    rows * K + G * N * K + 4 * rows * kb + 4 * G * nb * kb + 2 * rows * N, inp, (G, max_m, N),
+                    torch.bfloat16,
+                    (lambda em_: lambda d, o, s: dg.dg_m_grouped_masked(d["A"], d["sfa"], d["B"], d["sfb"], d["masked_m"], o,
+                                                                         expected_m=em_, stream=s))(em),
+                    lambda h, r: (O.m_grouped_masked(h["A"], h["sfa"], h["B"], h["sfb"], h["masked_m"],
+                                                     rows=list(range(min(r, int(h["masked_m"][0]))))),
+                                  2.0 * min(r, int(h["masked_m"][0])) * h["B"].shape[1] * h["B"].shape[2])[1]))
+    return cases
+
+
+def kgrouped_cases():
+    import moe_grouped_gemm_tma_gb300 as dg
+    from moe_grouped_gemm_tma_gb300 import inputs as I
+    from oracle import oracle as O
+    cases = []
+    for (M, N) in ((7168, 4096), (2048, 7168)):
+        for G in (4, 8):
+            seed = I.seed_for(4, G * 10 + M)
+            ks = I.kgrouped_sizes(seed, G, 4096)
+            c = I.make_kgrouped(seed, G, M, N, ks)
+            sumK = sum(ks)
+            inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb}
+            cases.append(Case(
+                f"G{G} M{M} N{N} sumK{sumK}", 2.0 * M * N * sumK,
+                (M + N) * sumK + 4 * (M + N) * sumK // 128 + 8 * G * M * N, inp, (G, M, N), torch.float32,
+                (lambda ks_: lambda d, o, s: dg.dg_k_grouped_wgrad(d["A"], d["sfa"], d["B"], d["sfb"], ks_, o, stream=s))(ks),
+                (lambda ks_: lambda h, r: (O.k_grouped_wgrad(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], ks_,
+                                                            np.zeros((len(ks_), r, h["B"].shape[0]), np.float32)),
+                                           2.0 * r * h["B"].shape[0] * sum(ks_))[1])(ks),
+                init_out=c.D_in))
+    return cases
+
+
+def build_cases(workload, shape=None):
+    if workload == "dense":
+        return dense_cases(shape)
+    return {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases}[workload]()
+
+
+def cpu_oracle_rate(cases, rows_per_case):
+    """Oracle TFLOP/s on the first `rows_per_case` rows of every case, all host threads."""
+    from oracle import oracle as O
+    host = [{k: v.cpu() for k, v in c.inputs.items()} for c in cases]
     total_flops, t0 = 0.0, time.perf_counter()
-    for (M, N, K) in SHAPES:
-        c = host[(N, K)]
-        r = min(rows_per_gemm, M)
-        O.gemm_fp8_nt(c.A[:r], c.sfa[:r], c.B, c.sfb)
-        total_flops += flops(r, N, K)
+    for c, h in zip(cases, host):
+        total_flops += c.oracle(h, rows_per_case)
     dt = time.perf_counter() - t0
     return total_flops / dt / 1e12, dt, total_flops, O.hardware_threads()
 
 
+# ------------------------------------------------------------------------------------------------ arms
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     from oracle import oracle as O
+    from moe_grouped_gemm_tma_gb300 import inputs as I
     O.build()
-    host = make_inputs()
+    cases = build_cases(args.workload, args.shape)
     for _ in range(args.warmup):
-        cpu_oracle_rate(host, REF_SAMPLE_ROWS)
-    times, fl = [], 0.0
+        cpu_oracle_rate(cases, REF_SAMPLE_ROWS)
+    times, fl, threads = [], 0.0, 0
     for _ in range(args.steps):
-        _, dt, fl, threads = cpu_oracle_rate(host, REF_SAMPLE_ROWS)
+        _, dt, fl, threads = cpu_oracle_rate(cases, REF_SAMPLE_ROWS)
         times.append(dt)
     total = sum(times)
     value = fl * args.steps / total / 1e12
-    sample = f"first {REF_SAMPLE_ROWS} rows of each of the 18 GEMMs per step ({fl / 1e9:.1f} GFLOP)"
+    sample = f"first {REF_SAMPLE_ROWS} rows of each of the {len(cases)} cases per step ({fl / 1e9:.1f} GFLOP)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": sample},
+        "config": {"workload": WORKLOADS[args.workload], "sample": sample},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -195,8 +301,14 @@ def run_reference(args):
     return 0
 
 
+def spin_cycles_for(host_step_s, steps):
+    # keep the GPU busy for longer than the host needs to enqueue every timed launch (capped at 2 s)
+    return int(min(2.0, 1.5 * host_step_s * (steps + 1) + 0.005) * 2.1e9)
+
+
 def run_ours(args):
     import moe_grouped_gemm_tma_gb300 as dg
+    from moe_grouped_gemm_tma_gb300 import inputs as I
 
     world, rank, local = dist_env()
     if world > 1:
@@ -209,21 +321,22 @@ def run_ours(args):
     dg.load()
     peaks, peak_kind = load_peaks()
 
-    host = make_inputs()
-    # device buffers: every GEMM gets its own copies (distinct addresses keep each run L2-cold)
+    I.set_generation_device(dev)
+    cases = build_cases(args.workload, args.shape)
+    I.set_generation_device("cpu")
+    # device buffers: every case its own copies (distinct addresses keep each run L2-cold)
     bufs = []
-    for (M, N, K) in SHAPES:
-        c = host[(N, K)]
-        bufs.append(dict(
-            shape=(M, N, K),
-            A=c.A[:M].to(dev), sfa=c.sfa[:M].to(dev), B=c.B.to(dev), sfb=c.sfb.to(dev),
-            D=torch.empty(M, N, dtype=torch.bfloat16, device=dev)))
+    for c in cases:
+        d = {k: v.to(dev).clone() for k, v in c.inputs.items()}
+        out = (c.init_out.to(dev).clone() if c.init_out is not None
+               else torch.empty(c.out_shape, dtype=c.out_dtype, device=dev))
+        bufs.append((d, out))
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
     def step():
-        for b in bufs:
-            dg.dg_gemm_fp8_nt(b["A"], b["sfa"], b["B"], b["sfb"], b["D"], stream=stream)
+        for c, (d, out) in zip(cases, bufs):
+            c.call(d, out, stream)
 
     host_s = []
     for _ in range(max(args.warmup, 0)):
@@ -233,22 +346,18 @@ def run_ours(args):
         host_s.append(time.perf_counter() - t0)
     if dg.dg_device_status(stream) != 0:
         raise RuntimeError("device-side timeout during warm-up")
-    # Small GEMMs run for a few microseconds, less than the host needs to enqueue one call, so the GPU
-    # is first kept busy by a spin kernel for longer than the host takes to enqueue every timed launch;
-    # the events then measure device time only (the e2e figure below keeps the host in the loop).
-    enqueue_s = (min(host_s) if host_s else 0.01) * (args.steps + 1)
-    spin_cycles = int(min(2.0, 1.5 * enqueue_s + 0.005) * 2.1e9)
+    host_step = min(host_s) if host_s else 0.01
 
-    n = len(bufs)
+    n = len(cases)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index)
     time.sleep(0.3)
-    # timed region: K steps back to back, only a start and a stop event (events between launches would
-    # serialise them and hide the overlap of one GEMM's set-up with the previous one's tail)
-    torch.cuda._sleep(spin_cycles)
+    # timed region: K steps back to back between one start and one stop event (events between launches
+    # would serialise them and hide the overlap of one GEMM's set-up with the previous one's tail)
+    torch.cuda._sleep(spin_cycles_for(host_step, args.steps))
     start.record(stream)
     for _ in range(args.steps):
         step()
@@ -264,67 +373,62 @@ def run_ours(args):
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
+    step_flops = sum(c.flops for c in cases)
+    value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
 
-    # per-launch breakdown (roofline of the dominant kernel): a second pass with an event after every
-    # launch, also behind a spin kernel
+    # per-case breakdown: a second pass with an event after every launch, also behind a spin kernel
     prof_steps = max(1, min(args.steps, 20))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(prof_steps)]
     torch.cuda.synchronize()
-    torch.cuda._sleep(int(min(2.0, 1.5 * (min(host_s) if host_s else 0.01) * (prof_steps + 1) + 0.005) * 2.1e9))
+    torch.cuda._sleep(spin_cycles_for(host_step, prof_steps))
     for s_ in range(prof_steps):
         ev[s_][0].record(stream)
-        for i, b in enumerate(bufs):
-            dg.dg_gemm_fp8_nt(b["A"], b["sfa"], b["B"], b["sfb"], b["D"], stream=stream)
+        for i, (c, (d, out)) in enumerate(zip(cases, bufs)):
+            c.call(d, out, stream)
             ev[s_][i + 1].record(stream)
     torch.cuda.synchronize()
-    per_launch = np.array([[ev[s_][i].elapsed_time(ev[s_][i + 1]) for i in range(n)] for s_ in range(prof_steps)])
-    avg_ms = per_launch.mean(axis=0)
-    step_flops = sum(flops(*b["shape"]) for b in bufs)
-    value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    avg_ms = np.array([[ev[s_][i].elapsed_time(ev[s_][i + 1]) for i in range(n)] for s_ in range(prof_steps)]).mean(axis=0)
 
-    per_shape = []
-    for i, b in enumerate(bufs):
-        M, N, K = b["shape"]
-        t_roof, bound = roofline_time(M, N, K, peaks)
-        per_shape.append({"M": M, "N": N, "K": K, "ms": round(float(avg_ms[i]), 5),
-                          "tflops": round(flops(M, N, K) / (avg_ms[i] * 1e-3) / 1e12, 1),
-                          "gbs": round(algo_bytes(M, N, K) / (avg_ms[i] * 1e-3) / 1e9, 1),
-                          "bound": bound, "roofline_frac": round(t_roof / (avg_ms[i] * 1e-3), 3)})
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    bw = peaks["hbm_gbs"]
+    per_case = []
+    for i, c in enumerate(cases):
+        t_tc, t_bw = c.flops / (fp8_peak * 1e12), c.bytes / (bw * 1e9)
+        per_case.append({"case": c.name, "ms": round(float(avg_ms[i]), 5),
+                         "tflops": round(c.flops / (avg_ms[i] * 1e-3) / 1e12, 1),
+                         "gbs": round(c.bytes / (avg_ms[i] * 1e-3) / 1e9, 1),
+                         "bound": "tensor" if t_tc >= t_bw else "hbm",
+                         "roofline_frac": round(max(t_tc, t_bw) / (avg_ms[i] * 1e-3), 3)})
     dom = int(np.argmax(avg_ms))
-    M, N, K = bufs[dom]["shape"]
-    _, bound = roofline_time(M, N, K, peaks)
-    if bound == "tensor":
-        achieved = flops(M, N, K) / (avg_ms[dom] * 1e-3) / 1e12
-        peak = 2.0 * peaks["bf16_tflops_sustained"]
-        unit = "TFLOP/s"
+    c = cases[dom]
+    if per_case[dom]["bound"] == "tensor":
+        achieved, peak, unit, src = c.flops / (avg_ms[dom] * 1e-3) / 1e12, fp8_peak, "TFLOP/s", "2 x bf16_tflops_sustained"
     else:
-        achieved = algo_bytes(M, N, K) / (avg_ms[dom] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    roofline = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic((M, N, K)),
-                "kernel": f"dg_gemm_kernel normal M={M} N={N} K={K}",
-                "peak_source": f"{peak_kind} ({'2 x bf16_tflops_sustained' if bound == 'tensor' else 'hbm_gbs'})",
-                "share": round(float(avg_ms[dom] / avg_ms.sum()), 3)}
+        achieved, peak, unit, src = c.bytes / (avg_ms[dom] * 1e-3) / 1e9, bw, "GB/s", "hbm_gbs"
+    roofline = {"bound": per_case[dom]["bound"], "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(c.name),
+                "kernel": f"dg_gemm_kernel, {args.workload} case {c.name}",
+                "peak_source": f"{peak_kind} ({src})", "share": round(float(avg_ms[dom] / avg_ms.sum()), 3)}
 
     # end to end through the public API with host buffers: pinned H2D of every input, the call, D2H
-    pinned = []
-    h2d = d2h = 0
-    for (M, N, K) in SHAPES:
-        c = host[(N, K)]
-        hb = dict(A=c.A[:M].contiguous().pin_memory(), sfa=c.sfa[:M].contiguous().pin_memory(),
-                  B=c.B.pin_memory(), sfb=c.sfb.pin_memory(),
-                  D=torch.empty(M, N, dtype=torch.bfloat16).pin_memory())
-        h2d += sum(hb[k].numel() * hb[k].element_size() for k in ("A", "sfa", "B", "sfb"))
-        d2h += hb["D"].numel() * hb["D"].element_size()
+    pinned, h2d, d2h = [], 0, 0
+    for c in cases:
+        hb = {k: v.cpu().contiguous().pin_memory() for k, v in c.inputs.items()}
+        if c.init_out is not None:
+            hb["__out_in"] = c.init_out.cpu().contiguous().pin_memory()
+        hb["__out"] = torch.empty(c.out_shape, dtype=c.out_dtype).pin_memory()
+        h2d += sum(v.numel() * v.element_size() for k, v in hb.items() if k != "__out")
+        d2h += hb["__out"].numel() * hb["__out"].element_size()
         pinned.append(hb)
 
     def e2e_step():
-        for b, hb in zip(bufs, pinned):
-            for k in ("A", "sfa", "B", "sfb"):
-                b[k].copy_(hb[k], non_blocking=True)
-            dg.dg_gemm_fp8_nt(b["A"], b["sfa"], b["B"], b["sfb"], b["D"], stream=stream)
-            hb["D"].copy_(b["D"], non_blocking=True)
+        for c, (d, out), hb in zip(cases, bufs, pinned):
+            for k in c.inputs:
+                d[k].copy_(hb[k], non_blocking=True)
+            if "__out_in" in hb:
+                out.copy_(hb["__out_in"], non_blocking=True)
+            c.call(d, out, stream)
+            hb["__out"].copy_(out, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 3))):
         e2e_step()
@@ -346,27 +450,27 @@ def run_ours(args):
     e2e_value = step_flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
 
     if rank == 0:
-        cpu_tf, cpu_s, cpu_fl, threads = cpu_oracle_rate(host, CPU_SAMPLE_ROWS)
+        cpu_tf, cpu_s, cpu_fl, threads = cpu_oracle_rate(cases, CPU_SAMPLE_ROWS)
+        label = WORKLOADS[args.workload] if args.shape is None else f"single dense GEMM M,N,K = {args.shape}"
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-            "config": {"workload": WORKLOAD if len(SHAPES) > 1 else f"single GEMM M,N,K = {SHAPES[0]}",
-                       "gemms_per_step": n,
-                       "l2": "inputs larger than L2: each GEMM has its own buffers, ~1.5 GB per step in all",
+            "config": {"workload": label, "cases_per_step": n,
+                       "l2": "inputs larger than L2: every case has its own buffers, far above L2 per step",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "timing": "device time: CUDA events around the K steps, enqueued behind a GPU spin "
-                                 "kernel so host launch cost is excluded (e2e includes it); per_shape and "
+                                 "kernel so host launch cost is excluded (e2e includes it); per_case and "
                                  "roofline from a second pass with an event after every launch"},
             "roofline": roofline,
             "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"first {CPU_SAMPLE_ROWS} rows of each of the 18 GEMMs "
+                             "sample": f"first {CPU_SAMPLE_ROWS} rows of each of the {n} cases "
                                        f"({cpu_fl / 1e9:.1f} GFLOP in {cpu_s:.1f} s)"},
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "clocks": clk,
             "gpu_launches": n * args.steps,
-            "per_shape": per_shape,
+            "per_case": per_case,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -377,15 +481,16 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
     ap.add_argument("--shape", default=None,
-                    help="M,N,K: time only this GEMM of the workload (for profiler captures)")
+                    help="M,N,K: time only this GEMM of the dense workload (for profiler captures)")
     args = ap.parse_args()
     if args.shape:
-        global SHAPES
-        SHAPES = [tuple(int(x) for x in args.shape.split(","))]
+        args.shape = tuple(int(x) for x in args.shape.split(","))
+        args.workload = "dense"
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

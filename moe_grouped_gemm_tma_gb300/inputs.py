@@ -89,6 +89,42 @@ def normals(seed: int, count: int) -> np.ndarray:
     return out
 
 
+def _t_shr(x: torch.Tensor, k: int) -> torch.Tensor:
+    """Logical right shift of int64 bit patterns (torch's >> is arithmetic)."""
+    return (x >> k) & ((1 << (64 - k)) - 1)
+
+
+def _u64_as_i64(v: int) -> int:
+    v &= 0xFFFFFFFFFFFFFFFF
+    return v - (1 << 64) if v >= (1 << 63) else v
+
+
+def normals_torch(seed: int, count: int, device) -> torch.Tensor:
+    """The same ``count`` normals as :func:`normals`, computed with torch ops on ``device`` (int64
+    arithmetic wraps modulo 2**64 exactly like the uint64 definition; shifts are made logical)."""
+    out = torch.empty(count, dtype=torch.float32, device=device)
+    pairs = (count + 1) // 2
+    g, m1, m2 = _u64_as_i64(0x9E3779B97F4A7C15), _u64_as_i64(0xBF58476D1CE4E5B9), _u64_as_i64(0x94D049BB133111EB)
+    sd = _u64_as_i64(int(seed))
+    step = 1 << 24
+    for p0 in range(0, pairs, step):
+        npair = min(step, pairs - p0)
+        idx = torch.arange(2 * p0 + 1, 2 * p0 + 2 * npair + 1, dtype=torch.int64, device=device)
+        z = sd + idx * g
+        z = (z ^ _t_shr(z, 30)) * m1
+        z = (z ^ _t_shr(z, 27)) * m2
+        z = z ^ _t_shr(z, 31)
+        u = (_t_shr(z, 11).to(torch.float64) + 1.0) * (2.0 ** -53)
+        u = u.reshape(npair, 2)
+        r = torch.sqrt(-2.0 * torch.log(u[:, 0]))
+        th = (2.0 * math.pi) * u[:, 1]
+        zz = torch.stack([r * torch.cos(th), r * torch.sin(th)], dim=1).reshape(-1)
+        lo = 2 * p0
+        n = min(2 * npair, count - lo)
+        out[lo:lo + n] = zz[:n].to(torch.float32)
+    return out
+
+
 def _to_e4m3_bytes(x: torch.Tensor) -> torch.Tensor:
     x = x.clamp(-E4M3_MAX, E4M3_MAX)
     return x.to(torch.float8_e4m3fn).view(torch.uint8)
@@ -119,7 +155,20 @@ def quantize_128x128(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
     return q.contiguous(), s.contiguous()
 
 
+# Where the matrices are drawn: "cpu" (numpy, the definition) or a torch device (same values).
+_GEN_DEVICE = "cpu"
+
+
+def set_generation_device(device) -> None:
+    """Draw subsequent inputs on ``device`` (e.g. "cuda") with :func:`normals_torch`; "cpu" restores
+    the numpy path. The values are the same either way."""
+    global _GEN_DEVICE
+    _GEN_DEVICE = str(device)
+
+
 def _normal_matrix(seed: int, stream: int, rows: int, cols: int) -> torch.Tensor:
+    if _GEN_DEVICE != "cpu":
+        return normals_torch(_stream_seed(seed, stream), rows * cols, _GEN_DEVICE).reshape(rows, cols)
     return torch.from_numpy(normals(_stream_seed(seed, stream), rows * cols)).reshape(rows, cols)
 
 
@@ -175,7 +224,7 @@ def make_contiguous(seed: int, G: int, N: int, K: int, group_m: list) -> Contigu
     Mt = sum(seg)
     A, sfa = quantize_1x128(_normal_matrix(seed, STREAM_A, Mt, K)) if Mt else (
         torch.zeros(0, K, dtype=torch.uint8), torch.zeros(0, K // BLOCK, dtype=torch.float32))
-    m_idx = torch.full((Mt,), -1, dtype=torch.int32)
+    m_idx = torch.full((Mt,), -1, dtype=torch.int32, device=A.device)
     r = 0
     for g, (m, s) in enumerate(zip(group_m, seg)):
         m_idx[r:r + m] = g
@@ -216,7 +265,7 @@ def make_masked(seed: int, G: int, max_m: int, N: int, K: int, masked_m: list, e
         Bs.append(b)
         sfbs.append(sb)
     return MaskedCase(G, max_m, N, K, expected_m, A.reshape(G, max_m, K), sfa.reshape(G, max_m, K // BLOCK),
-                      torch.stack(Bs), torch.stack(sfbs), torch.tensor(masked_m, dtype=torch.int32))
+                      torch.stack(Bs), torch.stack(sfbs), torch.tensor(masked_m, dtype=torch.int32, device=A.device))
 
 
 @dataclass

@@ -324,3 +324,12 @@ def test_kgrouped_g1_equals_dense_definition():
     ex = exact_gemm(c.A.numpy(), c.sfa.numpy(), c.B.numpy(), c.sfb.numpy(), sfb_per_row=True)
     want = np.array([[np.float32(float(v)) for v in row] for row in ex], dtype=np.float32)
     np.testing.assert_array_equal(got[0], want)
+
+
+# ----------------------------------------------------------------------------------------- generator
+def test_torch_generator_matches_numpy_definition():
+    # the bench may draw inputs with torch ops on the GPU; they must be the same numbers
+    for seed, n in ((I._stream_seed(5, 1), 1001), (I._stream_seed(0xD6E0, 2), 4097)):
+        a = I.normals(seed, n)
+        b = I.normals_torch(seed, n, "cpu").numpy()
+        np.testing.assert_array_equal(a, b)
