@@ -108,7 +108,7 @@ constexpr Spec kNormalSpecs2[] = {{128, 2}, {160, 2}, {192, 2}, {224, 2}, {256, 
 constexpr Spec kContiguousSpecs[] = {{128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
 constexpr Spec kMaskedSpecs1[] = {{64, 1}, {128, 1}, {192, 1}, {256, 1}};
 constexpr Spec kMaskedSpecs2[] = {{128, 2}, {256, 2}};
-constexpr Spec kKGroupedSpecs1[] = {{128, 1}};
+constexpr Spec kKGroupedSpecs1[] = {{128, 1}, {192, 1}};
 constexpr Spec kKGroupedSpecs2[] = {{128, 2}};
 
 // Pick BN minimising waves * (BN + per-tile overhead), ties to the larger BN: the time of one wave of
@@ -208,7 +208,7 @@ cudaError_t launch_spec<kMasked>(Spec sp, const Launch& L) {
 
 template <>
 cudaError_t launch_spec<kKGrouped>(Spec sp, const Launch& L) {
-    DG_CASE(kKGrouped, 128, 1) DG_CASE(kKGrouped, 128, 2)
+    DG_CASE(kKGrouped, 128, 1) DG_CASE(kKGrouped, 192, 1) DG_CASE(kKGrouped, 128, 2)
     return cudaErrorInvalidValue;
 }
 #undef DG_CASE

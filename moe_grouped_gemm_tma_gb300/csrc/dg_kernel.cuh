@@ -526,17 +526,22 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 // in two alternating register buffers: group g+1's TMEM loads are in flight while group g
                 // is promoted. The accumulator is released right after its last load has completed,
                 // before the last group's FMAs; the scale slot after the FMAs that read it.
-                constexpr int NG = (CHUNKS + 1) / 2;
-                uint32_t rb[2][2][16];
-                tmem_ld_x16(taddr, rb[0][0]);
-                if (CHUNKS > 1) tmem_ld_x16(taddr + 16, rb[0][1]);
+                // chunks per group: two (32 columns), or one for the k-grouped layout at wide tiles,
+                // whose per-column scales need the registers
+                constexpr int GC = (MODE == kKGrouped && COLS > 96) ? 1 : 2;
+                constexpr int NG = (CHUNKS + GC - 1) / GC;
+                uint32_t rb[2][GC][16];
+#pragma unroll
+                for (int cc = 0; cc < GC; ++cc)
+                    if (cc < CHUNKS) tmem_ld_x16(taddr + cc * 16, rb[0][cc]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int g = 0; g < NG; ++g) {
                     const int b = g & 1;
                     if (g + 1 < NG) {
-                        tmem_ld_x16(taddr + (g + 1) * 32, rb[b ^ 1][0]);
-                        if (2 * (g + 1) + 1 < CHUNKS) tmem_ld_x16(taddr + (g + 1) * 32 + 16, rb[b ^ 1][1]);
+#pragma unroll
+                        for (int cc = 0; cc < GC; ++cc)
+                            if ((g + 1) * GC + cc < CHUNKS) tmem_ld_x16(taddr + ((g + 1) * GC + cc) * 16, rb[b ^ 1][cc]);
                     } else {
                         tc_fence_before();
                         __syncwarp();
@@ -547,8 +552,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         }
                     }
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * g + cc;
+                    for (int cc = 0; cc < GC; ++cc) {
+                        const int c = GC * g + cc;
                         if (c >= CHUNKS) break;
                         const uint32_t* r = rb[b][cc];
                         if (MODE == kKGrouped) {

@@ -132,10 +132,12 @@ def run_kgrouped(c):
     return D.cpu().numpy()
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("bn,pair", [(0, 1), (128, 1), (192, 1), (0, 2)])
 @pytest.mark.parametrize("ks,M,N", [([256, 0, 384], 200, 264), ([128], 128, 128), ([512, 128, 1024, 256], 300, 1000)])
-def test_kgrouped_small_full_parity(ks, M, N, pair, monkeypatch):
+def test_kgrouped_small_full_parity(ks, M, N, bn, pair, monkeypatch):
     monkeypatch.setenv("DG_PAIR", str(pair))
+    if bn:
+        monkeypatch.setenv("DG_BN", str(bn))
     c = I.make_kgrouped(I.seed_for(4, sum(ks) + M), len(ks), M, N, ks)
     got = run_kgrouped(c)
     want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in)
