@@ -147,6 +147,20 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time, on every rank (the job ends when its last replica does)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops, steps, world, ms):
+    """Whole-job throughput: every replica ran `steps` steps of `step_flops` within `ms`."""
+    return step_flops * steps * world / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------------------------------------ cases
 class Case:
     """One GEMM of a workload: its inputs (on the generation device), work counts and calls."""
@@ -254,10 +268,16 @@ def kgrouped_cases():
     return cases
 
 
-def build_cases(workload, shape=None):
+def build_cases(workload, shape=None, only=None):
     if workload == "dense":
-        return dense_cases(shape)
-    return {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases}[workload]()
+        cases = dense_cases(shape)
+    else:
+        cases = {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases}[workload]()
+    if only:
+        cases = [c for c in cases if only in c.name]
+        if not cases:
+            raise SystemExit(f"no case of the {workload} workload matches {only!r}")
+    return cases
 
 
 def cpu_oracle_rate(cases, rows_per_case):
@@ -279,7 +299,7 @@ def run_reference(args):
     from oracle import oracle as O
     from moe_grouped_gemm_tma_gb300 import inputs as I
     O.build()
-    cases = build_cases(args.workload, args.shape)
+    cases = build_cases(args.workload, args.shape, args.case)
     for _ in range(args.warmup):
         cpu_oracle_rate(cases, REF_SAMPLE_ROWS)
     times, fl, threads = [], 0.0, 0
@@ -322,7 +342,7 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
 
     I.set_generation_device(dev)
-    cases = build_cases(args.workload, args.shape)
+    cases = build_cases(args.workload, args.shape, args.case)
     I.set_generation_device("cpu")
     # device buffers: every case its own copies (distinct addresses keep each run L2-cold)
     bufs = []
@@ -368,13 +388,9 @@ def run_ours(args):
     clk = clocks.stop()
     if dg.dg_device_status(stream) != 0:
         raise RuntimeError("device-side timeout in the timed region")
-    total_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     step_flops = sum(c.flops for c in cases)
-    value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = job_tflops(step_flops, args.steps, world, total_ms)
 
     # per-case breakdown: a second pass with an event after every launch, also behind a spin kernel
     prof_steps = max(1, min(args.steps, 20))
@@ -442,12 +458,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = step_flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tflops(step_flops, e2e_steps, world, e2e_ms)
 
     if rank == 0:
         cpu_tf, cpu_s, cpu_fl, threads = cpu_oracle_rate(cases, CPU_SAMPLE_ROWS)
@@ -487,6 +499,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
     ap.add_argument("--shape", default=None,
                     help="M,N,K: time only this GEMM of the dense workload (for profiler captures)")
+    ap.add_argument("--case", default=None,
+                    help="time only the cases of the workload whose name contains this text (for profiler captures)")
     args = ap.parse_args()
     if args.shape:
         args.shape = tuple(int(x) for x in args.shape.split(","))

@@ -53,7 +53,7 @@ constexpr int THREADS = 128 + 32 * EPI_WARPS;
 constexpr int CTRL_REGS = 56;           // registers per thread of warpgroup 0 after setmaxnreg
 constexpr int EPI_REGS = 224;           // ... of the epilogue warpgroups (128*56 + 256*224 = 384*168)
 constexpr int TMEM_COLS = 512;
-constexpr int SCALE_SLOTS = 16;
+constexpr int SCALE_SLOTS_MAX = 16;
 constexpr int MAX_MASKED_G = 1024;
 constexpr int MAX_KGROUPS = 128;
 constexpr int SMEM_LIMIT = 232448;      // 227 KB per CTA on sm_100-family parts
@@ -82,6 +82,15 @@ struct Params {
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
+// Deepest operand ring (at most 8 stages) whose dynamic layout -- alignment slack, ring and scale slots
+// rounded up to 1 KB, output staging -- fits next to the static shared memory.
+constexpr int ring_stages(int stage_bytes, int scale_bytes, int store_bytes, int static_bytes) {
+    int s = 8;
+    while (s > 1 && 1024 + ((s * stage_bytes + scale_bytes + 1023) / 1024) * 1024 + store_bytes + static_bytes > SMEM_LIMIT)
+        --s;
+    return s;
+}
+
 template <int MODE, int BN, int PAIR>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
@@ -94,13 +103,15 @@ struct Cfg {
     // scale slot: sfa of the CTA's 128 rows, then sfb: 4 block rows (from n0/128), or BN per-row values
     static constexpr int SB = (MODE == kKGrouped) ? BN : 4;
     static constexpr int SLOT_FLOATS = BM + SB;
+    // the k-grouped slots hold BN per-column values, so they get a shallower ring
+    static constexpr int SCALE_SLOTS = (MODE == kKGrouped) ? 8 : SCALE_SLOTS_MAX;
     static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
-    // output staging for TMA stores: per epilogue warp two 1 KB boxes of 32 rows x 16 BF16 columns
-    static constexpr bool TMA_STORE = (MODE != kKGrouped);
-    static constexpr int STORE_BYTES = TMA_STORE ? EPI_WARPS * 2048 : 0;
-    static constexpr int STATIC_RESERVE = 1024 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - SCALE_BYTES - 1024 - STORE_BYTES - STATIC_RESERVE) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    // output staging for TMA stores: per epilogue warp two 1 KB boxes of 32 rows x 32 bytes (16 BF16
+    // columns, or 8 FP32 columns added into the k-grouped output)
+    static constexpr int STORE_BYTES = EPI_WARPS * 2048;
+    // static shared memory: barriers and flags (under 640 bytes), plus the masked prefix table
+    static constexpr int STATIC_RESERVE = 640 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
+    static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
     static constexpr int NACC = NACC_FIT > 8 ? 8 : NACC_FIT;
     static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + SCALE_BYTES + 1023) / 1024) * 1024;
@@ -238,7 +249,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ uint64_t tmem_full_bar[NACC], tmem_empty_bar[NACC];
-    __shared__ uint64_t scale_full_bar[SCALE_SLOTS], scale_empty_bar[SCALE_SLOTS];
+    __shared__ uint64_t scale_full_bar[C::SCALE_SLOTS], scale_empty_bar[C::SCALE_SLOTS];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_prefix[MODE == kMasked ? MAX_MASKED_G + 1 : 1];
@@ -273,7 +284,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             mbar_init(&tmem_full_bar[a], 1);
             mbar_init(&tmem_empty_bar[a], EPI_WARPS * PAIR);
         }
-        for (int s = 0; s < SCALE_SLOTS; ++s) {
+        for (int s = 0; s < C::SCALE_SLOTS; ++s) {
             mbar_init(&scale_full_bar[s], 32);
             mbar_init(&scale_empty_bar[s], EPI_WARPS);
         }
@@ -462,7 +473,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         cp_async_4(dst + BM + lane, sfb_src + kb);
                     }
                     cp_async_arrive_noinc(&scale_full_bar[slot]);
-                    if (++slot == SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                    if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
                 }
                 if (!ok) break;
             }
@@ -490,21 +501,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             const int bidx = cstart / 128 - ti.n0 / 128;
             const int split = (128 * (cstart / 128 + 1) - cstart) / 16;   // chunks before the next block
 
+            // the k-grouped output is accumulated by the TMA's add at the tile's end, so every layout
+            // starts the tile's sum at zero
             float accum[COLS];
-            if (MODE == kKGrouped) {
-                const float* drow = reinterpret_cast<const float*>(p.d) +
-                                    static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
-                const bool row_ok = row_in_tile < ti.rows_valid;
 #pragma unroll
-                for (int j = 0; j < COLS; j += 4) {
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (row_ok && cstart + j < p.n) v = *reinterpret_cast<const float4*>(drow + j);
-                    accum[j] = v.x; accum[j + 1] = v.y; accum[j + 2] = v.z; accum[j + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < COLS; ++j) accum[j] = 0.f;
-            }
+            for (int j = 0; j < COLS; ++j) accum[j] = 0.f;
 
             for (int kb = 0; kb < ti.nkb; ++kb) {
                 const bool got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
@@ -590,7 +591,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
                 if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
-                if (++slot == SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
             }
             if (!ok) break;
 
@@ -603,7 +604,32 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 continue;
             }
             // ---- store this CTA's rows of the tile
-            if (C::TMA_STORE && (MODE != kMasked || ti.rows_valid >= BM)) {
+            if (MODE == kKGrouped) {
+                // D[g] += tile: FP32 boxes of 32 rows x 8 columns, added element-wise by the TMA (one
+                // add per element, so the result does not depend on timing); the three-dimensional
+                // map [G][M][N] skips rows past M and columns past N
+                uint8_t* wbuf = s_store + ew * 2048;
+                const int y = ti.m0 + q * 32;
+                const int sw = (lane >> 2) & 1;
+#pragma unroll
+                for (int c = 0; c < COLS / 8; ++c) {
+                    uint8_t* half = wbuf + (store_round & 1u) * 1024;
+                    ++store_round;
+                    if (lane == 0) bulk_wait_read_1();
+                    __syncwarp();
+                    uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
+                    rowp[sw] = make_uint4(__float_as_uint(accum[c * 8 + 0]), __float_as_uint(accum[c * 8 + 1]),
+                                          __float_as_uint(accum[c * 8 + 2]), __float_as_uint(accum[c * 8 + 3]));
+                    rowp[sw ^ 1] = make_uint4(__float_as_uint(accum[c * 8 + 4]), __float_as_uint(accum[c * 8 + 5]),
+                                              __float_as_uint(accum[c * 8 + 6]), __float_as_uint(accum[c * 8 + 7]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_3d(&tmap_d, half, cstart + c * 8, y, ti.g);
+                        bulk_commit();
+                    }
+                }
+            } else if (MODE != kMasked || ti.rows_valid >= BM) {
                 // Stage 32 rows x 16 columns per round in one of the warp's two 1 KB halves (32-byte
                 // swizzle: a row's two 16-byte chunks swap places every 4 rows, so the warp's stores
                 // hit all banks), then one lane issues the TMA store of the box; TMA clips rows and
@@ -630,22 +656,14 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     }
                 }
             } else if (row_in_tile < ti.rows_valid) {
-                if (MODE == kKGrouped) {
-                    float* drow = reinterpret_cast<float*>(p.d) + static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
+                // a masked tile with rows past masked_m: plain stores of the valid rows only
+                __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.d) +
+                                      static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
 #pragma unroll
-                    for (int j = 0; j < COLS; j += 4)
-                        if (cstart + j < p.n)
-                            st_global_v4(drow + j, __float_as_uint(accum[j]), __float_as_uint(accum[j + 1]),
-                                         __float_as_uint(accum[j + 2]), __float_as_uint(accum[j + 3]));
-                } else {
-                    __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.d) +
-                                          static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
-#pragma unroll
-                    for (int j = 0; j < COLS; j += 8)
-                        if (cstart + j < p.n)
-                            st_global_v4(drow + j, pack_bf16x2(accum[j], accum[j + 1]), pack_bf16x2(accum[j + 2], accum[j + 3]),
-                                         pack_bf16x2(accum[j + 4], accum[j + 5]), pack_bf16x2(accum[j + 6], accum[j + 7]));
-                }
+                for (int j = 0; j < COLS; j += 8)
+                    if (cstart + j < p.n)
+                        st_global_v4(drow + j, pack_bf16x2(accum[j], accum[j + 1]), pack_bf16x2(accum[j + 2], accum[j + 3]),
+                                     pack_bf16x2(accum[j + 4], accum[j + 5]), pack_bf16x2(accum[j + 6], accum[j + 7]));
             }
         }
         // every TMA store of this warp has completed (and released its staging buffer) before exit

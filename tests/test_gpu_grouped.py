@@ -132,7 +132,7 @@ def run_kgrouped(c):
     return D.cpu().numpy()
 
 
-@pytest.mark.parametrize("bn,pair", [(0, 1), (128, 1), (192, 1), (0, 2)])
+@pytest.mark.parametrize("bn,pair", [(0, 1), (128, 1), (192, 1), (224, 1), (256, 1), (0, 2)])
 @pytest.mark.parametrize("ks,M,N", [([256, 0, 384], 200, 264), ([128], 128, 128), ([512, 128, 1024, 256], 300, 1000)])
 def test_kgrouped_small_full_parity(ks, M, N, bn, pair, monkeypatch):
     monkeypatch.setenv("DG_PAIR", str(pair))
