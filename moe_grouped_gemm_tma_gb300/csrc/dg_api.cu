@@ -128,7 +128,9 @@ constexpr Spec kKGroupedSpecs2[] = {{128, 2}};
 
 // Pick BN minimising waves * (BN + per-tile overhead), ties to the larger BN: the time of one wave of
 // (128 * PAIR) x BN tiles grows with BN, and the number of waves is the tile count over the number of
-// tiles that run at once (SMs / PAIR).
+// tiles that run at once (SMs / PAIR). The overhead term (96 columns' worth) is the measured cost of a
+// narrower tile: each 128-K block still stages and feeds the whole 128-row A tile and pays the same
+// epilogue round trip, so a BN=160 tile takes well over 160/256 of a BN=256 tile's time.
 template <size_t NC>
 Spec choose_spec(const Spec (&cands)[NC], int64_t row_units, int n, int sms) {
     Spec best = cands[NC - 1];
@@ -138,7 +140,7 @@ Spec choose_spec(const Spec (&cands)[NC], int64_t row_units, int n, int sms) {
         const int64_t slots = sms / cands[i].pair;
         const int64_t tiles = row_units * cdiv(n, bn);
         const int64_t waves = (tiles + slots - 1) / slots;
-        const int64_t cost = waves * (bn + 16);
+        const int64_t cost = waves * (bn + 96);
         if (cost <= best_cost) { best_cost = cost; best = cands[i]; }
     }
     return best;

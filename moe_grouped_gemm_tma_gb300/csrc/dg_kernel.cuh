@@ -111,13 +111,25 @@ struct Cfg {
     static constexpr int STORE_BYTES = EPI_WARPS * 2048;
     // static shared memory: barriers and flags (under 640 bytes), plus the masked prefix table
     static constexpr int STATIC_RESERVE = 640 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
-    static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES, STORE_BYTES, STATIC_RESERVE);
+    // Narrow tiles: the two epilogue warpgroups take alternate K blocks over all BN columns (two
+    // independent per-block chains in flight) instead of one column half each; once per tile each hands
+    // the other the half it does not store, through XCHG_BYTES of shared memory.
+    static constexpr bool KPAR = (BN <= 64 && MODE != kKGrouped);
+    static constexpr int XCHG_BYTES = KPAR ? 2 * BM * (BN / 2) * 4 : 0;
+    static constexpr int EPI_ARRIVALS = KPAR ? EPI_WARPS / 2 : EPI_WARPS;   // warps releasing one block
+    static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
     static constexpr int NACC = NACC_FIT > 8 ? 8 : NACC_FIT;
-    static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + SCALE_BYTES + 1023) / 1024) * 1024;
+    static constexpr int XCHG_OFF = STAGES * STAGE_BYTES + SCALE_BYTES;
+    static constexpr int STORE_OFF = ((XCHG_OFF + XCHG_BYTES + 1023) / 1024) * 1024;
     static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
     static constexpr int COLS = BN / 2;        // columns per epilogue warpgroup
     static constexpr int CHUNKS = COLS / 16;   // 16-column TMEM loads per K block
+    // Epilogue TMEM loads per K block come in batches of EPI_GC chunks, each batch waited on once.
+    // Double-buffered (EPI_DB): batch g+1 is in flight while batch g is promoted. Single-buffered:
+    // larger batches in the same registers, so fewer load round trips per block.
+    static constexpr int EPI_GC = (MODE == kKGrouped && COLS > 96) ? 1 : 2;
+    static constexpr bool EPI_DB = true;
     // split-K partial sums: [128 rows][BN + 4] FP32 (padded rows: conflict-free 16-byte stores), in the
     // operand ring, which is idle once the tile's last MMA has completed
     static constexpr int PSTRIDE = BN + 4;
@@ -235,6 +247,38 @@ __device__ __forceinline__ float pick4(const float4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// Promotion of one 16-column chunk c of a K block's partial sums r into the running sums:
+// acc += r * s (s = sfa * sfb of the chunk's 128-column block), or, with per-column scales (k-grouped),
+// acc += (r * scol[n]) * sa.
+template <int MODE, int COLS>
+__device__ __forceinline__ void promote_chunk(float (&accum)[COLS], const uint32_t* r, int c, float s, float sa,
+                                              const float* scol) {
+    if (MODE == kKGrouped) {
+        const float2 sa2 = make_float2(sa, sa);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const float4 sv = *reinterpret_cast<const float4*>(scol + c * 16 + j);
+            float2 a0 = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
+            float2 a1 = make_float2(accum[c * 16 + j + 2], accum[c * 16 + j + 3]);
+            const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), make_float2(sv.x, sv.y));
+            const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), make_float2(sv.z, sv.w));
+            a0 = __ffma2_rn(p0, sa2, a0);
+            a1 = __ffma2_rn(p1, sa2, a1);
+            accum[c * 16 + j] = a0.x; accum[c * 16 + j + 1] = a0.y;
+            accum[c * 16 + j + 2] = a1.x; accum[c * 16 + j + 3] = a1.y;
+        }
+    } else {
+        const float2 s2 = make_float2(s, s);
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            float2 a = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
+            a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2, a);
+            accum[c * 16 + j] = a.x;
+            accum[c * 16 + j + 1] = a.y;
+        }
+    }
+}
+
 template <int MODE, int BN, int PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -250,6 +294,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ uint64_t tmem_full_bar[NACC], tmem_empty_bar[NACC];
     __shared__ uint64_t scale_full_bar[C::SCALE_SLOTS], scale_empty_bar[C::SCALE_SLOTS];
+    __shared__ uint64_t xchg_full_bar, xchg_free_bar;   // narrow-tile partial-sum exchange
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
     __shared__ int s_prefix[MODE == kMasked ? MAX_MASKED_G + 1 : 1];
@@ -274,6 +319,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     uint8_t* smem_b = smem + STAGES * C::A_BYTES;
     float* s_scales = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
     uint8_t* s_store = smem + C::STORE_OFF;
+    float* s_xchg = reinterpret_cast<float*>(smem + C::XCHG_OFF);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -282,11 +328,15 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(&tmem_full_bar[a], 1);
-            mbar_init(&tmem_empty_bar[a], EPI_WARPS * PAIR);
+            mbar_init(&tmem_empty_bar[a], C::EPI_ARRIVALS * PAIR);
         }
         for (int s = 0; s < C::SCALE_SLOTS; ++s) {
             mbar_init(&scale_full_bar[s], 32);
-            mbar_init(&scale_empty_bar[s], EPI_WARPS);
+            mbar_init(&scale_empty_bar[s], C::EPI_ARRIVALS);
+        }
+        {
+            mbar_init(&xchg_full_bar, EPI_WARPS);
+            mbar_init(&xchg_free_bar, EPI_WARPS);
         }
         s_abort = 0;
         fence_mbar_init();
@@ -406,8 +456,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    const bool got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status) &&
-                                     wait_bounded(&full_bar[stage], phase, abort_flag, p.status);
+                    bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_empty_bar[acc], acc_phase ^ 1u)) &
+                                static_cast<unsigned>(mbar_try_wait(&full_bar[stage], phase))) != 0u;
+                    if (!got)
+                        got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status) &&
+                              wait_bounded(&full_bar[stage], phase, abort_flag, p.status);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -488,6 +541,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         const int h = ew >> 2;                 // column half of the tile
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * COLS;
+        uint32_t xphase = 0;                   // narrow-tile exchange rounds so far (parity)
         int acc = 0, slot = 0;
         uint32_t acc_phase = 0, sphase = 0;
         uint32_t store_round = 0;              // TMA-store boxes issued so far (staging half parity)
@@ -507,91 +561,150 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 #pragma unroll
             for (int j = 0; j < COLS; ++j) accum[j] = 0.f;
 
-            for (int kb = 0; kb < ti.nkb; ++kb) {
-                const bool got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
-                                 wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
-                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t taddr = lane_addr + static_cast<uint32_t>(acc * BN);
-                const float* sl = s_scales + slot * C::SLOT_FLOATS;
-                const float sa = sl[row_in_tile];
-                float s0 = 0.f, s1 = 0.f;
-                if (MODE != kKGrouped) {
-                    const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
-                    s0 = sa * pick4(b4, bidx);
-                    s1 = sa * pick4(b4, bidx + 1 < 4 ? bidx + 1 : 3);
-                }
-                const float* scol = sl + BM + h * COLS;   // k-grouped per-column scales
+            if constexpr (!C::KPAR) {
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    // both barriers are probed at once (each try_wait is a round trip to shared memory);
+                    // only an incomplete one falls back to the bounded waits
+                    bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_full_bar[acc], acc_phase)) &
+                                static_cast<unsigned>(mbar_try_wait(&scale_full_bar[slot], sphase))) != 0u;
+                    if (!got)
+                        got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
+                              wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t taddr = lane_addr + static_cast<uint32_t>(acc * BN);
+                    const float* sl = s_scales + slot * C::SLOT_FLOATS;
+                    const float sa = sl[row_in_tile];
+                    float s0 = 0.f, s1 = 0.f;
+                    if (MODE != kKGrouped) {
+                        const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
+                        s0 = sa * pick4(b4, bidx);
+                        s1 = sa * pick4(b4, bidx + 1 < 4 ? bidx + 1 : 3);
+                    }
+                    const float* scol = sl + BM + h * COLS;   // k-grouped per-column scales
 
-                // Loads and promotion are software-pipelined over groups of 32 columns (two x16 loads)
-                // in two alternating register buffers: group g+1's TMEM loads are in flight while group g
-                // is promoted. The accumulator is released right after its last load has completed,
-                // before the last group's FMAs; the scale slot after the FMAs that read it.
-                // chunks per group: two (32 columns), or one for the k-grouped layout at wide tiles,
-                // whose per-column scales need the registers
-                constexpr int GC = (MODE == kKGrouped && COLS > 96) ? 1 : 2;
-                constexpr int NG = (CHUNKS + GC - 1) / GC;
-                uint32_t rb[2][GC][16];
-#pragma unroll
-                for (int cc = 0; cc < GC; ++cc)
-                    if (cc < CHUNKS) tmem_ld_x16(taddr + cc * 16, rb[0][cc]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int g = 0; g < NG; ++g) {
-                    const int b = g & 1;
-                    if (g + 1 < NG) {
+                    // TMEM loads and promotion in batches of GC chunks (see Cfg). The accumulator is released
+                    // right after its last load has completed, before the last batch's FMAs; the scale slot
+                    // after the FMAs that read it.
+                    constexpr int GC = C::EPI_GC;
+                    constexpr bool DB = C::EPI_DB;
+                    constexpr int NG = (CHUNKS + GC - 1) / GC;
+                    uint32_t rb[DB ? 2 : 1][GC][16];
+                    if (DB) {
 #pragma unroll
                         for (int cc = 0; cc < GC; ++cc)
-                            if ((g + 1) * GC + cc < CHUNKS) tmem_ld_x16(taddr + ((g + 1) * GC + cc) * 16, rb[b ^ 1][cc]);
-                    } else {
+                            if (cc < CHUNKS) tmem_ld_x16(taddr + cc * 16, rb[0][cc]);
+                        tmem_ld_wait();
+                    }
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        const int b = DB ? (g & 1) : 0;
+                        if (!DB) {
+#pragma unroll
+                            for (int cc = 0; cc < GC; ++cc)
+                                if (g * GC + cc < CHUNKS) tmem_ld_x16(taddr + (g * GC + cc) * 16, rb[0][cc]);
+                            tmem_ld_wait();
+                        } else if (g + 1 < NG) {
+#pragma unroll
+                            for (int cc = 0; cc < GC; ++cc)
+                                if ((g + 1) * GC + cc < CHUNKS) tmem_ld_x16(taddr + ((g + 1) * GC + cc) * 16, rb[b ^ 1][cc]);
+                        }
+                        if (g + 1 == NG) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                // the accumulator is released on the leader's barrier (the peer's is unused)
+                                if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
+                                else mbar_arrive(&tmem_empty_bar[acc]);
+                            }
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < GC; ++cc) {
+                            const int c = GC * g + cc;
+                            if (c >= CHUNKS) break;
+                            promote_chunk<MODE, COLS>(accum, rb[b][cc], c, (c < split) ? s0 : s1, sa, scol);
+                        }
+                        if (DB && g + 1 < NG) tmem_ld_wait();
+                    }
+                    // every lane has read its scales (the FMAs above used them)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
+                    if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
+                    if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                }
+            } else {
+                // all BN columns of every other K block (this warpgroup's parity); the columns lie in one
+                // 128-column sfb block, since BN divides 128 and n0 is a multiple of BN
+                float accf[BN];
+#pragma unroll
+                for (int j = 0; j < BN; ++j) accf[j] = 0.f;
+                const uint32_t row_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    if ((kb & 1) == h) {
+                        bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_full_bar[acc], acc_phase)) &
+                                    static_cast<unsigned>(mbar_try_wait(&scale_full_bar[slot], sphase))) != 0u;
+                        if (!got)
+                            got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
+                                  wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
+                        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                        tc_fence_after();
+                        constexpr int NCH = BN / 16;
+                        uint32_t rb[NCH][16];
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) tmem_ld_x16(row_addr + static_cast<uint32_t>(acc * BN + c * 16), rb[c]);
+                        const float* sl = s_scales + slot * C::SLOT_FLOATS;
+                        const float sab = sl[row_in_tile] * sl[BM];
+                        tmem_ld_wait();
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
-                            // the accumulator is released on the leader's barrier (the peer's is unused)
                             if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
                             else mbar_arrive(&tmem_empty_bar[acc]);
                         }
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) promote_chunk<MODE, BN>(accf, rb[c], c, sab, 0.f, nullptr);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
                     }
-#pragma unroll
-                    for (int cc = 0; cc < GC; ++cc) {
-                        const int c = GC * g + cc;
-                        if (c >= CHUNKS) break;
-                        const uint32_t* r = rb[b][cc];
-                        if (MODE == kKGrouped) {
-                            const float2 sa2 = make_float2(sa, sa);
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4) {
-                                const float4 sv = *reinterpret_cast<const float4*>(scol + c * 16 + j);
-                                float2 a0 = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
-                                float2 a1 = make_float2(accum[c * 16 + j + 2], accum[c * 16 + j + 3]);
-                                const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                                             make_float2(sv.x, sv.y));
-                                const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                                                             make_float2(sv.z, sv.w));
-                                a0 = __ffma2_rn(p0, sa2, a0);
-                                a1 = __ffma2_rn(p1, sa2, a1);
-                                accum[c * 16 + j] = a0.x; accum[c * 16 + j + 1] = a0.y;
-                                accum[c * 16 + j + 2] = a1.x; accum[c * 16 + j + 3] = a1.y;
-                            }
-                        } else {
-                            const float s = (c < split) ? s0 : s1;
-                            const float2 s2 = make_float2(s, s);
-#pragma unroll
-                            for (int j = 0; j < 16; j += 2) {
-                                float2 a = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
-                                a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2, a);
-                                accum[c * 16 + j] = a.x;
-                                accum[c * 16 + j + 1] = a.y;
-                            }
-                        }
-                    }
-                    if (g + 1 < NG) tmem_ld_wait();
+                    if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
+                    if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
                 }
-                // every lane has read its scales (the FMAs above used them)
+                if (!ok) break;
+                // Exchange: warpgroup h stores columns [h*BN/2, (h+1)*BN/2) and hands the other half to
+                // the other warpgroup. Region h holds the half written by warpgroup h, rows of BN/2 floats
+                // in 16-byte chunks swizzled by row (chunk ^ (row & 7)), so neither side bank-conflicts.
+                constexpr int HC = BN / 8;   // 16-byte chunks per half row
+                const bool freed = wait_bounded(&xchg_free_bar, xphase ^ 1u, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, freed)) { ok = false; break; }
+                // split by h with compile-time indices only (so accf stays in registers)
+                float send[COLS], keep[COLS];
+                if (h == 0) {
+#pragma unroll
+                    for (int j = 0; j < COLS; ++j) { send[j] = accf[COLS + j]; keep[j] = accf[j]; }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < COLS; ++j) { send[j] = accf[j]; keep[j] = accf[COLS + j]; }
+                }
+                float4* mine = reinterpret_cast<float4*>(s_xchg) + (h * BM + row_in_tile) * HC;
+#pragma unroll
+                for (int c = 0; c < HC; ++c)
+                    mine[c ^ (row_in_tile & (HC - 1))] = make_float4(send[c * 4], send[c * 4 + 1], send[c * 4 + 2], send[c * 4 + 3]);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
-                if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
-                if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                if (lane == 0) mbar_arrive(&xchg_full_bar);
+                const bool full = wait_bounded(&xchg_full_bar, xphase, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, full)) { ok = false; break; }
+                const float4* theirs = reinterpret_cast<const float4*>(s_xchg) + ((1 - h) * BM + row_in_tile) * HC;
+#pragma unroll
+                for (int c = 0; c < HC; ++c) {
+                    const float4 v = theirs[c ^ (row_in_tile & (HC - 1))];
+                    accum[c * 4 + 0] = keep[c * 4 + 0] + v.x;
+                    accum[c * 4 + 1] = keep[c * 4 + 1] + v.y;
+                    accum[c * 4 + 2] = keep[c * 4 + 2] + v.z;
+                    accum[c * 4 + 3] = keep[c * 4 + 3] + v.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xchg_free_bar);
+                xphase ^= 1u;
             }
             if (!ok) break;
 
