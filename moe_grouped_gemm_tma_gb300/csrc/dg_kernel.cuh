@@ -128,6 +128,11 @@ struct Cfg {
     // Epilogue TMEM loads per K block come in batches of EPI_GC chunks, each batch waited on once.
     // Double-buffered (EPI_DB): batch g+1 is in flight while batch g is promoted. Single-buffered:
     // larger batches in the same registers, so fewer load round trips per block.
+    // Narrow tiles (four or more accumulators) and the k-grouped layout let the producer, the MMA issuer
+    // and the scale stager take a second K block in the same pass of their loops when it is ready
+    // already: a pass costs several hundred cycles of barrier round trips, more than the MMA of a narrow
+    // block. (Measured: it slows the wide two-accumulator tiles of the other layouts.)
+    static constexpr bool KB_PAIRING = (NACC >= 4) || MODE == kKGrouped;
     static constexpr int EPI_GC = (MODE == kKGrouped && COLS > 96) ? 1 : 2;
     static constexpr bool EPI_DB = true;
     // split-K partial sums: [128 rows][BN + 4] FP32 (padded rows: conflict-free 16-byte stores), in the
@@ -403,29 +408,43 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             for (int t = unit; t < num_tiles && ok; t += num_units) {
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
-                for (int kb = 0; kb < ti.nkb; ++kb) {
-                    const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                for (int kb = 0; kb < ti.nkb;) {
+                    // The next stage and, when the tile has another K block, the one after it are probed
+                    // at once; the second is filled in the same pass only if it is free already. (Each
+                    // pass of this loop costs several hundred cycles of barrier round trips, which
+                    // narrow tiles would otherwise pay per K block.)
+                    int s1 = stage + 1;
+                    uint32_t ph1 = phase;
+                    if (s1 == STAGES) { s1 = 0; ph1 ^= 1u; }
+                    const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
+                    const bool f0 = mbar_try_wait(&empty_bar[stage], phase ^ 1u);
+                    const bool f1 = more && mbar_test_wait(&empty_bar[s1], ph1 ^ 1u);
+                    const bool got = f0 || wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    const int x = (ti.kb0 + kb) * BK;
-                    uint8_t* a_dst = smem_a + stage * C::A_BYTES;
-                    uint8_t* b_dst = smem_b + stage * C::B_BYTES;
-                    if (PAIR == 1 || leader) {
-                        if (issuer) {
-                            mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
-                            tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
-                            tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                    const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
+                    for (int j = 0; j < take; ++j) {
+                        const int x = (ti.kb0 + kb + j) * BK;
+                        uint8_t* a_dst = smem_a + stage * C::A_BYTES;
+                        uint8_t* b_dst = smem_b + stage * C::B_BYTES;
+                        if (PAIR == 1 || leader) {
+                            if (issuer) {
+                                mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
+                                tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
+                                tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                            }
+                        } else {
+                            const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                            if (issuer) {
+                                tma_load_2d_pair(&tmap_a, bar, a_dst, x, ti.a_row);
+                                tma_load_2d_pair(&tmap_b, bar, b_dst, x, ti.b_row);
+                            }
                         }
-                    } else {
-                        const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
-                        if (issuer) {
-                            tma_load_2d_pair(&tmap_a, bar, a_dst, x, ti.a_row);
-                            tma_load_2d_pair(&tmap_b, bar, b_dst, x, ti.b_row);
-                        }
+                        issued |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     }
                     __syncwarp();
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    kb += take;
                 }
             }
             if (ok) {
@@ -455,41 +474,56 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             for (int t = unit; t < num_tiles && ok; t += num_units) {
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
-                for (int kb = 0; kb < ti.nkb; ++kb) {
-                    bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_empty_bar[acc], acc_phase ^ 1u)) &
-                                static_cast<unsigned>(mbar_try_wait(&full_bar[stage], phase))) != 0u;
+                for (int kb = 0; kb < ti.nkb;) {
+                    // This K block's accumulator and stage and, when the tile has another K block, the
+                    // next ones are probed at once; the second block is issued in the same pass only if it
+                    // is ready already (never waited for, so a two-accumulator tile keeps its overlap).
+                    int s1 = stage + 1, a1 = acc + 1;
+                    uint32_t ph1 = phase, ap1 = acc_phase;
+                    if (s1 == STAGES) { s1 = 0; ph1 ^= 1u; }
+                    if (a1 == NACC) { a1 = 0; ap1 ^= 1u; }
+                    const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
+                    const bool r0 = (static_cast<unsigned>(mbar_try_wait(&tmem_empty_bar[acc], acc_phase ^ 1u)) &
+                                     static_cast<unsigned>(mbar_try_wait(&full_bar[stage], phase))) != 0u;
+                    const bool r1 = more && (static_cast<unsigned>(mbar_test_wait(&tmem_empty_bar[a1], ap1 ^ 1u)) &
+                                             static_cast<unsigned>(mbar_test_wait(&full_bar[s1], ph1))) != 0u;
+                    bool got = r0;
                     if (!got)
                         got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status) &&
                               wait_bounded(&full_bar[stage], phase, abort_flag, p.status);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    const int take = __all_sync(0xffffffffu, r1) ? 2 : 1;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                    const uint64_t a_desc = sw128_kmajor_desc(a_base + stage * C::A_BYTES);
-                    const uint64_t b_desc = sw128_kmajor_desc(b_base + stage * C::B_BYTES);
-                    if (issuer) {
+                    for (int j = 0; j < take; ++j) {
+                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                        const uint64_t a_desc = sw128_kmajor_desc(a_base + stage * C::A_BYTES);
+                        const uint64_t b_desc = sw128_kmajor_desc(b_base + stage * C::B_BYTES);
+                        if (issuer) {
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            // advancing the start address by 32 bytes (>> 4 = 2) steps K by 32 within
-                            // the 128-byte swizzle row
-                            const uint64_t ad = a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
-                            const uint64_t bd = b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
-                            if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
-                            else mma_f8f6f4(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                            for (int k = 0; k < BK / UMMA_K; ++k) {
+                                // advancing the start address by 32 bytes (>> 4 = 2) steps K by 32 within
+                                // the 128-byte swizzle row
+                                const uint64_t ad = a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
+                                const uint64_t bd = b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
+                                if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                                else mma_f8f6f4(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                            }
+                            if (PAIR == 2) {
+                                mma_commit_pair(&empty_bar[stage], 0x3);
+                                mma_commit_pair(&tmem_full_bar[acc], 0x3);
+                            } else {
+                                mma_commit(&empty_bar[stage]);
+                                mma_commit(&tmem_full_bar[acc]);
+                            }
                         }
-                        if (PAIR == 2) {
-                            mma_commit_pair(&empty_bar[stage], 0x3);
-                            mma_commit_pair(&tmem_full_bar[acc], 0x3);
-                        } else {
-                            mma_commit(&empty_bar[stage]);
-                            mma_commit(&tmem_full_bar[acc]);
-                        }
+                        last_acc = acc;
+                        last_parity = acc_phase;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                        if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
                     }
                     __syncwarp();
                     any = true;
-                    last_acc = acc;
-                    last_parity = acc_phase;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
+                    kb += take;
                 }
             }
             if (!ok && any && issuer) drain_wait(&tmem_full_bar[last_acc], last_parity);
@@ -513,20 +547,32 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     sfb_src = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + blk) * p.kbs + ti.kb0;
                 }
                 bool ok = true;
-                for (int kb = 0; kb < ti.nkb; ++kb) {
-                    const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                for (int kb = 0; kb < ti.nkb;) {
+                    // as in the producer: a second slot is filled in the same pass if it is free already
+                    int s1 = slot + 1;
+                    uint32_t sp1 = sphase;
+                    if (s1 == C::SCALE_SLOTS) { s1 = 0; sp1 ^= 1u; }
+                    const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
+                    const bool f0 = mbar_try_wait(&scale_empty_bar[slot], sphase ^ 1u);
+                    const bool f1 = more && mbar_test_wait(&scale_empty_bar[s1], sp1 ^ 1u);
+                    const bool got = f0 || wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    float* dst = s_scales + slot * C::SLOT_FLOATS;
+                    const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
+                    for (int j = 0; j < take; ++j) {
+                        const int k = kb + j;
+                        float* dst = s_scales + slot * C::SLOT_FLOATS;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + kb);
-                    if (MODE == kKGrouped) {
-                        for (int j = lane; j < BN; j += 32)
-                            cp_async_4(dst + BM + j, sfb_src + static_cast<size_t>(min(ti.n0 + j, p.n - 1)) * p.kbs + kb);
-                    } else if (lane < 4) {
-                        cp_async_4(dst + BM + lane, sfb_src + kb);
+                        for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + k);
+                        if (MODE == kKGrouped) {
+                            for (int c = lane; c < BN; c += 32)
+                                cp_async_4(dst + BM + c, sfb_src + static_cast<size_t>(min(ti.n0 + c, p.n - 1)) * p.kbs + k);
+                        } else if (lane < 4) {
+                            cp_async_4(dst + BM + lane, sfb_src + k);
+                        }
+                        cp_async_arrive_noinc(&scale_full_bar[slot]);
+                        if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
                     }
-                    cp_async_arrive_noinc(&scale_full_bar[slot]);
-                    if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                    kb += take;
                 }
                 if (!ok) break;
             }
