@@ -7,7 +7,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -28,6 +30,7 @@ struct DeviceInfo {
     bool ready = false;
     bool supported = false;
     int sms = 0;
+    int l2_bytes = 0;
     int* status = nullptr;
 };
 DeviceInfo g_devices[kMaxDevices];
@@ -39,13 +42,15 @@ dg_status device_info(DeviceInfo* out) {
     std::lock_guard<std::mutex> lock(g_devices_mutex);
     DeviceInfo& d = g_devices[dev];
     if (!d.ready) {
-        int major = 0, minor = 0, sms = 0;
+        int major = 0, minor = 0, sms = 0, l2 = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
             return DG_CUDA_ERROR;
         d.supported = (major == 10 && minor == 3);
         d.sms = sms;
+        d.l2_bytes = l2;
         if (d.supported) {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return DG_CUDA_ERROR;
@@ -155,6 +160,26 @@ Spec spec_override(const Spec (&cands)[NC], Spec chosen) {
     for (size_t i = 0; i < NC; ++i)
         if (cands[i].bn == v) return cands[i];
     return chosen;
+}
+
+// Tile raster for the normal and contiguous layouts: bands of group_m row blocks, row block fastest
+// within a band. A band's A rows (group_m * 128 * PAIR * K bytes, at most a third of L2) stay resident
+// while the band sweeps every column block; with the plain row-fastest order a wave spans up to 152 row
+// blocks of one column block, and once A outgrows L2 every column block re-reads A from DRAM (measured
+// on the contiguous layout with 31k rows, K = 7168: 803 us row-fastest, 691 us in bands of 16).
+// DG_GROUP_M=<n> forces the band height for sweeps.
+int choose_group_m(int m_blocks, int tile_m, int64_t k, const DeviceInfo& dev) {
+    int gm = std::min(m_blocks, 16);
+    const int64_t band_bytes = static_cast<int64_t>(tile_m) * k;
+    if (band_bytes > 0 && dev.l2_bytes > 0) {
+        const int64_t fit = (static_cast<int64_t>(dev.l2_bytes) / 3) / band_bytes;
+        gm = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(fit, gm)));
+    }
+    if (const char* e = getenv("DG_GROUP_M")) {
+        const int v = atoi(e);
+        if (v > 0) gm = std::min(v, m_blocks);
+    }
+    return std::max(gm, 1);
 }
 
 // Split-K for problems whose tiles cannot fill half the SMs (small M): a cluster of S CTAs shares a
@@ -309,6 +334,7 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
     p.sfb_rows = cdiv(N, 128);
     p.m_blocks = cdiv(M, BM * sp.pair);
     p.n_blocks = cdiv(N, bn);
+    p.group_m = choose_group_m(p.m_blocks, BM * sp.pair, K, dev);
     p.split = split;
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
@@ -354,6 +380,7 @@ dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint
     p.groups = G;
     p.sfb_rows = cdiv(N, 128);
     p.m_blocks = Mt / BM;
+    p.group_m = choose_group_m(p.m_blocks, BM, K, dev);
     p.n_blocks = cdiv(N, bn);
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;

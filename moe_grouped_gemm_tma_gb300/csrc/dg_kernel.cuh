@@ -23,14 +23,21 @@
 //   warp 2      scale stager: per K block, cp.async copies of the block's sfa column (this CTA's 128
 //               rows) and the sfb values the tile needs into a SCALE_SLOTS-deep shared ring, running
 //               ahead of the epilogue so no scale load latency reaches it.
-//   warps 4..11 promotion / epilogue (two warpgroups, registers raised with setmaxnreg): the
-//               warpgroups split the BN columns; each thread owns one tile row (its TMEM lane) and
-//               BN/2 FP32 running sums. Per K block they read the block partial out of TMEM (64
-//               columns per wait), multiply by sfa[m,kb] * sfb and add (packed f32x2 FMA), and release
-//               the accumulator (`tmem_empty` in the leader) and the scale slot. At the end of a tile
-//               they round to BF16 (or add into FP32 for the weight gradient) and store.
+//   warps 4..11 promotion / epilogue (two warpgroups, registers raised with setmaxnreg): each thread
+//               owns one tile row (its TMEM lane). Per K block a thread reads the block partial out of
+//               TMEM, releases the accumulator (`tmem_empty` in the leader) as soon as its loads have
+//               completed, multiplies by sfa[m,kb] * sfb and adds into FP32 running sums (packed f32x2
+//               FMA), then releases the scale slot. Wide tiles: the warpgroups split the BN columns.
+//               Narrow tiles (BN <= 64): each warpgroup takes every other K block over all columns,
+//               and the two partial sums are exchanged once per tile through shared memory. At the
+//               end of a tile they round to BF16 and TMA-store 32 x 16 boxes, or TMA-add 32 x 8 FP32
+//               boxes into the weight gradient.
 // The MMA of K block kb+1.. overlaps the promotion of block kb (NACC accumulators in flight), and the
-// store of one tile overlaps the first MMAs of the next.
+// store of one tile overlaps the first MMAs of the next. Small-M GEMMs split K over a cluster of CTAs
+// and reduce the FP32 partials through distributed shared memory.
+//
+// Barrier round trips cost about a hundred cycles each, so the loops probe all barriers of a pass at
+// once, and on narrow tiles the producer, MMA issuer and stager take a second ready K block per pass.
 //
 // Every wait is bounded: after WAIT_LIMIT_NS a waiter records DG_DEVICE_TIMEOUT in the status word,
 // raises a CTA-wide abort flag, and the CTA drains its own in-flight copies and MMAs (bounded too),
@@ -79,6 +86,7 @@ struct Params {
     int n_blocks;              // ceil(n / BN)
     int tiles;                 // tile count when known on the host (not masked)
     int split;                 // normal layout, single-CTA tiles: CTAs (a cluster) sharing one tile's K
+    int group_m;               // normal / contiguous: row blocks per raster band (row block fastest)
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
@@ -113,9 +121,10 @@ struct Cfg {
     static constexpr int STATIC_RESERVE = 640 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
     // Narrow tiles: the two epilogue warpgroups take alternate K blocks over all BN columns (two
     // independent per-block chains in flight) instead of one column half each; once per tile each hands
-    // the other the half it does not store, through XCHG_BYTES of shared memory.
+    // the other the half it does not store, XCHG_PASS columns at a time through shared memory.
     static constexpr bool KPAR = (BN <= 64 && MODE != kKGrouped);
-    static constexpr int XCHG_BYTES = KPAR ? 2 * BM * (BN / 2) * 4 : 0;
+    static constexpr int XCHG_PASS = (BN / 2) < 32 ? (BN / 2) : 32;
+    static constexpr int XCHG_BYTES = KPAR ? 2 * BM * XCHG_PASS * 4 : 0;
     static constexpr int EPI_ARRIVALS = KPAR ? EPI_WARPS / 2 : EPI_WARPS;   // warps releasing one block
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
@@ -163,7 +172,12 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
     ti.kb0 = 0;
     ti.nkb = p.kbs;
     if (MODE == kNormal || MODE == kContiguous) {
-        const int mb = t % p.m_blocks, nb = t / p.m_blocks;
+        // bands of group_m row blocks; within a band the row block varies fastest
+        const int band_tiles = p.group_m * p.n_blocks;
+        const int band = t / band_tiles, r = t - band * band_tiles;
+        const int m_first = band * p.group_m;
+        const int gm = min(p.group_m, p.m_blocks - m_first);
+        const int mb = m_first + r % gm, nb = r / gm;
         ti.m0 = mb * TILE_M + rank * BM;
         ti.n0 = nb * BN;
         ti.a_row = ti.m0;
@@ -679,8 +693,9 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
                 }
             } else {
-                // all BN columns of every other K block (this warpgroup's parity); the columns lie in one
-                // 128-column sfb block, since BN divides 128 and n0 is a multiple of BN
+                // all BN columns of every other K block (this warpgroup's parity); outside the k-grouped
+                // layout the columns lie in one 128-column sfb block (BN divides 128, n0 is a multiple
+                // of BN), so one scale sfa * sfb serves the row
                 float accf[BN];
 #pragma unroll
                 for (int j = 0; j < BN; ++j) accf[j] = 0.f;
@@ -694,21 +709,31 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                                   wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
                         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                         tc_fence_after();
+                        // TMEM loads in batches of up to 64 columns (the registers next to BN running
+                        // sums), each waited on once; the accumulator is released after the last batch
                         constexpr int NCH = BN / 16;
-                        uint32_t rb[NCH][16];
-#pragma unroll
-                        for (int c = 0; c < NCH; ++c) tmem_ld_x16(row_addr + static_cast<uint32_t>(acc * BN + c * 16), rb[c]);
+                        constexpr int LB = NCH < 4 ? NCH : 4;
                         const float* sl = s_scales + slot * C::SLOT_FLOATS;
-                        const float sab = sl[row_in_tile] * sl[BM];
-                        tmem_ld_wait();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
-                            else mbar_arrive(&tmem_empty_bar[acc]);
-                        }
+                        const float sa = sl[row_in_tile];
+                        const float sab = (MODE == kKGrouped) ? 0.f : sa * sl[BM];
 #pragma unroll
-                        for (int c = 0; c < NCH; ++c) promote_chunk<MODE, BN>(accf, rb[c], c, sab, 0.f, nullptr);
+                        for (int b = 0; b < NCH / LB; ++b) {
+                            uint32_t rb[LB][16];
+#pragma unroll
+                            for (int c = 0; c < LB; ++c)
+                                tmem_ld_x16(row_addr + static_cast<uint32_t>(acc * BN + (b * LB + c) * 16), rb[c]);
+                            tmem_ld_wait();
+                            if (b + 1 == NCH / LB) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
+                                    else mbar_arrive(&tmem_empty_bar[acc]);
+                                }
+                            }
+#pragma unroll
+                            for (int c = 0; c < LB; ++c) promote_chunk<MODE, BN>(accf, rb[c], b * LB + c, sab, sa, sl + BM);
+                        }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
                     }
@@ -717,11 +742,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 }
                 if (!ok) break;
                 // Exchange: warpgroup h stores columns [h*BN/2, (h+1)*BN/2) and hands the other half to
-                // the other warpgroup. Region h holds the half written by warpgroup h, rows of BN/2 floats
-                // in 16-byte chunks swizzled by row (chunk ^ (row & 7)), so neither side bank-conflicts.
-                constexpr int HC = BN / 8;   // 16-byte chunks per half row
-                const bool freed = wait_bounded(&xchg_free_bar, xphase ^ 1u, abort_flag, p.status);
-                if (!__all_sync(0xffffffffu, freed)) { ok = false; break; }
+                // the other warpgroup, XCHG_PASS columns per pass. Region h holds what warpgroup h wrote:
+                // rows of XCHG_PASS floats in 16-byte chunks swizzled by row (chunk ^ (row & 7)), so
+                // neither side bank-conflicts.
+                constexpr int PASS = C::XCHG_PASS;
+                constexpr int HC = PASS / 4;   // 16-byte chunks per row and pass
                 // split by h with compile-time indices only (so accf stays in registers)
                 float send[COLS], keep[COLS];
                 if (h == 0) {
@@ -732,25 +757,33 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     for (int j = 0; j < COLS; ++j) { send[j] = accf[j]; keep[j] = accf[COLS + j]; }
                 }
                 float4* mine = reinterpret_cast<float4*>(s_xchg) + (h * BM + row_in_tile) * HC;
-#pragma unroll
-                for (int c = 0; c < HC; ++c)
-                    mine[c ^ (row_in_tile & (HC - 1))] = make_float4(send[c * 4], send[c * 4 + 1], send[c * 4 + 2], send[c * 4 + 3]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xchg_full_bar);
-                const bool full = wait_bounded(&xchg_full_bar, xphase, abort_flag, p.status);
-                if (!__all_sync(0xffffffffu, full)) { ok = false; break; }
                 const float4* theirs = reinterpret_cast<const float4*>(s_xchg) + ((1 - h) * BM + row_in_tile) * HC;
 #pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    const float4 v = theirs[c ^ (row_in_tile & (HC - 1))];
-                    accum[c * 4 + 0] = keep[c * 4 + 0] + v.x;
-                    accum[c * 4 + 1] = keep[c * 4 + 1] + v.y;
-                    accum[c * 4 + 2] = keep[c * 4 + 2] + v.z;
-                    accum[c * 4 + 3] = keep[c * 4 + 3] + v.w;
+                for (int ps = 0; ps < COLS / PASS; ++ps) {
+                    const bool freed = wait_bounded(&xchg_free_bar, xphase ^ 1u, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, freed)) { ok = false; break; }
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        const int j = ps * PASS + c * 4;
+                        mine[c ^ (row_in_tile & (HC - 1))] = make_float4(send[j], send[j + 1], send[j + 2], send[j + 3]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xchg_full_bar);
+                    const bool full = wait_bounded(&xchg_full_bar, xphase, abort_flag, p.status);
+                    if (!__all_sync(0xffffffffu, full)) { ok = false; break; }
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        const float4 v = theirs[c ^ (row_in_tile & (HC - 1))];
+                        const int j = ps * PASS + c * 4;
+                        accum[j + 0] = keep[j + 0] + v.x;
+                        accum[j + 1] = keep[j + 1] + v.y;
+                        accum[j + 2] = keep[j + 2] + v.z;
+                        accum[j + 3] = keep[j + 3] + v.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xchg_free_bar);
+                    xphase ^= 1u;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xchg_free_bar);
-                xphase ^= 1u;
             }
             if (!ok) break;
 
