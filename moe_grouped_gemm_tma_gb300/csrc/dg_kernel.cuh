@@ -114,9 +114,10 @@ struct Cfg {
     // the k-grouped slots hold BN per-column values, so they get a shallower ring
     static constexpr int SCALE_SLOTS = (MODE == kKGrouped) ? 8 : SCALE_SLOTS_MAX;
     static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
-    // output staging for TMA stores: per epilogue warp two 1 KB boxes of 32 rows x 32 bytes (16 BF16
+    // output staging for TMA stores: per epilogue warp STORE_SLOTS 1 KB boxes of 32 rows x 32 bytes (16 BF16
     // columns, or 8 FP32 columns added into the k-grouped output)
-    static constexpr int STORE_BYTES = EPI_WARPS * 2048;
+    static constexpr int STORE_SLOTS = 2;                        // 1 KB boxes in flight per epilogue warp
+    static constexpr int STORE_BYTES = EPI_WARPS * STORE_SLOTS * 1024;
     // static shared memory: barriers and flags (under 640 bytes), plus the masked prefix table
     static constexpr int STATIC_RESERVE = 640 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
     // Narrow tiles: the two epilogue warpgroups take alternate K blocks over all BN columns (two
@@ -148,7 +149,8 @@ struct Cfg {
     // operand ring, which is idle once the tile's last MMA has completed
     static constexpr int PSTRIDE = BN + 4;
     static constexpr int PARTIAL_BYTES = BM * PSTRIDE * 4;
-    static_assert(PARTIAL_BYTES <= STAGES * STAGE_BYTES, "split-K partials must fit in the operand ring");
+    static_assert(!(MODE == kNormal && PAIR == 1) || PARTIAL_BYTES <= STAGES * STAGE_BYTES,
+                  "split-K partials must fit in the operand ring");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte swizzle-atom alignment");
 };
@@ -604,7 +606,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         uint32_t xphase = 0;                   // narrow-tile exchange rounds so far (parity)
         int acc = 0, slot = 0;
         uint32_t acc_phase = 0, sphase = 0;
-        uint32_t store_round = 0;              // TMA-store boxes issued so far (staging half parity)
+        uint32_t store_round = 0;              // TMA-store boxes issued so far (picks the staging slot)
         bool ok = true;
 
         for (int t = unit; t < num_tiles && ok; t += num_units) {
@@ -800,14 +802,14 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 // D[g] += tile: FP32 boxes of 32 rows x 8 columns, added element-wise by the TMA (one
                 // add per element, so the result does not depend on timing); the three-dimensional
                 // map [G][M][N] skips rows past M and columns past N
-                uint8_t* wbuf = s_store + ew * 2048;
+                uint8_t* wbuf = s_store + ew * (C::STORE_SLOTS * 1024);
                 const int y = ti.m0 + q * 32;
                 const int sw = (lane >> 2) & 1;
 #pragma unroll
                 for (int c = 0; c < COLS / 8; ++c) {
-                    uint8_t* half = wbuf + (store_round & 1u) * 1024;
+                    uint8_t* half = wbuf + (store_round % C::STORE_SLOTS) * 1024;
                     ++store_round;
-                    if (lane == 0) bulk_wait_read_1();
+                    if (lane == 0) bulk_wait_read_n<C::STORE_SLOTS - 1>();
                     __syncwarp();
                     uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
                     rowp[sw] = make_uint4(__float_as_uint(accum[c * 8 + 0]), __float_as_uint(accum[c * 8 + 1]),
@@ -822,18 +824,18 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     }
                 }
             } else if (MODE != kMasked || ti.rows_valid >= BM) {
-                // Stage 32 rows x 16 columns per round in one of the warp's two 1 KB halves (32-byte
+                // Stage 32 rows x 16 columns per round in one of the warp's 1 KB slots (32-byte
                 // swizzle: a row's two 16-byte chunks swap places every 4 rows, so the warp's stores
                 // hit all banks), then one lane issues the TMA store of the box; TMA clips rows and
                 // columns outside D. A half is rewritten only after its previous box has been read.
-                uint8_t* wbuf = s_store + ew * 2048;
+                uint8_t* wbuf = s_store + ew * (C::STORE_SLOTS * 1024);
                 const int y = ti.d_row + q * 32;
                 const int sw = (lane >> 2) & 1;
 #pragma unroll
                 for (int c = 0; c < CHUNKS; ++c) {
-                    uint8_t* half = wbuf + (store_round & 1u) * 1024;
+                    uint8_t* half = wbuf + (store_round % C::STORE_SLOTS) * 1024;
                     ++store_round;
-                    if (lane == 0) bulk_wait_read_1();
+                    if (lane == 0) bulk_wait_read_n<C::STORE_SLOTS - 1>();
                     __syncwarp();
                     uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
                     rowp[sw] = make_uint4(pack_bf16x2(accum[c * 16 + 0], accum[c * 16 + 1]), pack_bf16x2(accum[c * 16 + 2], accum[c * 16 + 3]),
