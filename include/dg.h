@@ -105,6 +105,18 @@ dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* 
                              const int32_t* ks_host, float* D, int G, int M, int N,
                              cudaStream_t stream);
 
+/*
+ * Dense weight-gradient GEMM with FP32 output (pages: wgrad_gemm_fp8_fp8_fp32_nt; dW = X^T . dY of a
+ * dense layer in the backward pass). The single-expert case of dg_k_grouped_wgrad, plus an
+ * overwriting form:
+ *   A = X^T  [M, K]   e4m3        sfa [M, K/128]   (1x128 scales along K)
+ *   B = dY^T [N, K]   e4m3        sfb [N, K/128]   (1x128 scales along K, per row)
+ *   D        [M, N]   fp32: D += A . B^T if accumulate != 0, else D = A . B^T (old contents ignored)
+ * K must be a multiple of 128. K == 0 leaves D unchanged when accumulating and zeroes it otherwise.
+ */
+dg_status dg_wgrad_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
+                          float* D, int M, int N, int K, int accumulate, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* dg_status_string(dg_status status);
 

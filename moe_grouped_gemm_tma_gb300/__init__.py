@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "DGError", "load", "dg_gemm_fp8_nt", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
-    "dg_k_grouped_wgrad", "dg_device_status", "dg_status_string", "scale_shapes", "library_path",
+    "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status", "dg_status_string", "scale_shapes", "library_path",
 ]
 
 _lock = threading.Lock()
@@ -55,11 +55,12 @@ def load(build_if_missing: bool = True):
             L.dg_m_grouped_contiguous.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
             L.dg_m_grouped_masked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
             L.dg_k_grouped_wgrad.argtypes = [P, P, P, P, P, P, I, I, I, P]
+            L.dg_wgrad_fp8_nt.argtypes = [P, P, P, P, P, I, I, I, I, P]
             L.dg_device_status.argtypes = [P]
             L.dg_status_string.argtypes = [I]
             L.dg_status_string.restype = ctypes.c_char_p
             for f in ("dg_gemm_fp8_nt", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
-                      "dg_k_grouped_wgrad", "dg_device_status"):
+                      "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status"):
                 getattr(L, f).restype = I
             _lib = L
     return _lib
@@ -192,6 +193,23 @@ def dg_k_grouped_wgrad(A, sfa, B, sfb, ks, D, stream=None):
     st = load().dg_k_grouped_wgrad(_ptr(A), _ptr(sfa), _ptr(B), _ptr(sfb), ks_arr, _ptr(D), G, M, N,
                                    _stream(stream))
     _check(st, "dg_k_grouped_wgrad")
+    return D
+
+
+def dg_wgrad_fp8_nt(A, sfa, B, sfb, D, accumulate=True, stream=None):
+    """Dense FP32 weight gradient: D += A . B^T (accumulate) or D = A . B^T, 1x128 scales on both."""
+    A, B = _codes(A, "A"), _codes(B, "B")
+    sfa, sfb = _f32(sfa, "sfa"), _f32(sfb, "sfb")
+    D = _f32(D, "D")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    if tuple(sfa.shape) != (M, K // 128) or tuple(sfb.shape) != (N, K // 128):
+        raise ValueError("scale shape mismatch")
+    st = load().dg_wgrad_fp8_nt(_ptr(A), _ptr(sfa), _ptr(B), _ptr(sfb), _ptr(D), M, N, K,
+                                1 if accumulate else 0, _stream(stream))
+    _check(st, "dg_wgrad_fp8_nt")
     return D
 
 

@@ -267,6 +267,68 @@ dg_status common_prologue(DeviceInfo* dev) {
 
 using namespace dg;
 
+// Both weight-gradient entry points: experts g own consecutive K windows of widths ks_host[g]; the tile
+// is added into D (D += ...) or, with overwrite, stored (D = ...).
+static dg_status wgrad_impl(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
+                            const int32_t* ks_host, float* D, int G, int M, int N, bool overwrite,
+                            cudaStream_t stream) {
+    if (G < 0 || M < 0 || N < 0) return DG_INVALID_ARG;
+    if (G == 0 || M == 0 || N == 0) return DG_OK;
+    if (G > MAX_KGROUPS || !ks_host) return DG_INVALID_ARG;
+    int64_t sumK = 0;
+    for (int g = 0; g < G; ++g) {
+        if (ks_host[g] < 0) return DG_INVALID_ARG;
+        if (ks_host[g] % 128 != 0) return DG_UNSUPPORTED_SHAPE;
+        sumK += ks_host[g];
+    }
+    if (N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (sumK == 0) return DG_OK;
+    if (sumK > INT32_MAX || static_cast<int64_t>(G) * M > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    if (!A || !B || !sfa || !sfb || !D) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(sfa, 4) || !aligned(sfb, 4))
+        return DG_MISALIGNED;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+
+    const bool pair = use_pair(M);
+    const Spec sp = pair ? spec_override(kKGroupedSpecs2, choose_spec(kKGroupedSpecs2, static_cast<int64_t>(G) * cdiv(M, 2 * BM), N, dev.sms))
+                         : spec_override(kKGroupedSpecs1, choose_spec(kKGroupedAuto1, static_cast<int64_t>(G) * cdiv(M, BM), N, dev.sms));
+    const int bn = sp.bn;
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if (make_operand_map(&L.tmap_a, A, M, sumK, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, sumK, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
+    if (make_wgrad_map(&L.tmap_d, D, G, M, N) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.status = dev.status;
+    p.overwrite = overwrite ? 1 : 0;
+    p.rows = M;
+    p.n = N;
+    p.kbs = static_cast<int>(sumK / 128);
+    p.groups = G;
+    p.sfb_rows = N;
+    p.m_blocks = cdiv(M, BM * sp.pair);
+    p.n_blocks = cdiv(N, bn);
+    int off = 0;
+    for (int g = 0; g < G; ++g) {
+        p.kb_off[g] = off;
+        off += ks_host[g] / 128;
+    }
+    p.kb_off[G] = off;
+    const int64_t tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
+    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = static_cast<int>(tiles);
+    L.units = p.tiles;
+    L.sms = dev.sms;
+    L.stream = stream;
+    return launch_spec<kKGrouped>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
+
 extern "C" {
 
 const char* dg_status_string(dg_status s) {
@@ -442,59 +504,26 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
 
 dg_status dg_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,
                              const int32_t* ks_host, float* D, int G, int M, int N, cudaStream_t stream) {
-    if (G < 0 || M < 0 || N < 0) return DG_INVALID_ARG;
-    if (G == 0 || M == 0 || N == 0) return DG_OK;
-    if (G > MAX_KGROUPS || !ks_host) return DG_INVALID_ARG;
-    int64_t sumK = 0;
-    for (int g = 0; g < G; ++g) {
-        if (ks_host[g] < 0) return DG_INVALID_ARG;
-        if (ks_host[g] % 128 != 0) return DG_UNSUPPORTED_SHAPE;
-        sumK += ks_host[g];
-    }
-    if (N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
-    if (sumK == 0) return DG_OK;
-    if (sumK > INT32_MAX || static_cast<int64_t>(G) * M > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
-    if (!A || !B || !sfa || !sfb || !D) return DG_INVALID_ARG;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16) || !aligned(sfa, 4) || !aligned(sfb, 4))
-        return DG_MISALIGNED;
-    DeviceInfo dev;
-    dg_status st = common_prologue(&dev);
-    if (st != DG_OK) return st;
+    return wgrad_impl(A, sfa, B, sfb, ks_host, D, G, M, N, false, stream);
+}
 
-    const bool pair = use_pair(M);
-    const Spec sp = pair ? spec_override(kKGroupedSpecs2, choose_spec(kKGroupedSpecs2, static_cast<int64_t>(G) * cdiv(M, 2 * BM), N, dev.sms))
-                         : spec_override(kKGroupedSpecs1, choose_spec(kKGroupedAuto1, static_cast<int64_t>(G) * cdiv(M, BM), N, dev.sms));
-    const int bn = sp.bn;
-    Launch L;
-    std::memset(&L, 0, sizeof(L));
-    if (make_operand_map(&L.tmap_a, A, M, sumK, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_operand_map(&L.tmap_b, B, N, sumK, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
-    if (make_wgrad_map(&L.tmap_d, D, G, M, N) != DG_OK) return DG_CUDA_ERROR;
-    Params& p = L.params;
-    p.sfa = sfa;
-    p.sfb = sfb;
-    p.d = D;
-    p.status = dev.status;
-    p.rows = M;
-    p.n = N;
-    p.kbs = static_cast<int>(sumK / 128);
-    p.groups = G;
-    p.sfb_rows = N;
-    p.m_blocks = cdiv(M, BM * sp.pair);
-    p.n_blocks = cdiv(N, bn);
-    int off = 0;
-    for (int g = 0; g < G; ++g) {
-        p.kb_off[g] = off;
-        off += ks_host[g] / 128;
+dg_status dg_wgrad_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, float* D,
+                          int M, int N, int K, int accumulate, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
+    if (M == 0 || N == 0) return DG_OK;
+    if (K % 128 != 0 || N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (K == 0) {
+        if (accumulate) return DG_OK;
+        if (!D) return DG_INVALID_ARG;
+        if (!aligned(D, 16)) return DG_MISALIGNED;
+        DeviceInfo dev;
+        dg_status st = common_prologue(&dev);
+        if (st != DG_OK) return st;
+        return cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * sizeof(float), stream) == cudaSuccess
+                   ? DG_OK : DG_CUDA_ERROR;
     }
-    p.kb_off[G] = off;
-    const int64_t tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
-    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
-    p.tiles = static_cast<int>(tiles);
-    L.units = p.tiles;
-    L.sms = dev.sms;
-    L.stream = stream;
-    return launch_spec<kKGrouped>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    const int32_t ks[1] = {K};
+    return wgrad_impl(A, sfa, B, sfb, ks, D, 1, M, N, accumulate == 0, stream);
 }
 
 }  // extern "C"

@@ -87,6 +87,7 @@ struct Params {
     int tiles;                 // tile count when known on the host (not masked)
     int split;                 // normal layout, single-CTA tiles: CTAs (a cluster) sharing one tile's K
     int group_m;               // normal / contiguous: row blocks per raster band (row block fastest)
+    int overwrite;             // k-grouped: store the tile (D = ...) instead of adding it (D += ...)
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
@@ -800,8 +801,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             // ---- store this CTA's rows of the tile
             if (MODE == kKGrouped) {
                 // D[g] += tile: FP32 boxes of 32 rows x 8 columns, added element-wise by the TMA (one
-                // add per element, so the result does not depend on timing); the three-dimensional
-                // map [G][M][N] skips rows past M and columns past N
+                // add per element, so the result does not depend on timing), or stored (overwriting
+                // form); the three-dimensional map [G][M][N] skips rows past M and columns past N
                 uint8_t* wbuf = s_store + ew * (C::STORE_SLOTS * 1024);
                 const int y = ti.m0 + q * 32;
                 const int sw = (lane >> 2) & 1;
@@ -819,7 +820,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_reduce_add_3d(&tmap_d, half, cstart + c * 8, y, ti.g);
+                        if (p.overwrite) tma_store_3d(&tmap_d, half, cstart + c * 8, y, ti.g);
+                        else tma_reduce_add_3d(&tmap_d, half, cstart + c * 8, y, ti.g);
                         bulk_commit();
                     }
                 }

@@ -116,6 +116,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                  : "memory");
 }
 
+// 3-D tiled store of a box from shared memory (bulk-group completion); elements outside the tensor
+// are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+                 : "memory");
+}
+
 // Element-wise add of a shared-memory box into global memory (the add happens in L2); the element
 // type is the tensor map's. Elements outside the tensor are skipped.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {

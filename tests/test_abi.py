@@ -18,10 +18,10 @@ def declared_symbols():
     return sorted(set(re.findall(r"^\s*(?:dg_status|const char\*)\s+(dg_\w+)\s*\(", text, flags=re.M)))
 
 
-def test_header_declares_the_four_operations():
+def test_header_declares_every_operation():
     syms = declared_symbols()
     for s in ("dg_gemm_fp8_nt", "dg_m_grouped_contiguous", "dg_m_grouped_masked", "dg_k_grouped_wgrad",
-              "dg_status_string", "dg_device_status"):
+              "dg_wgrad_fp8_nt", "dg_status_string", "dg_device_status"):
         assert s in syms
 
 
@@ -65,6 +65,11 @@ def test_rejects_bad_shapes_before_any_cuda_call():
     assert L.dg_k_grouped_wgrad(ok, ok, ok, ok, ks, ok, 2, 8, 8, None) == 1
     ks = (ctypes.c_int32 * 2)(0, 0)
     assert L.dg_k_grouped_wgrad(ok, ok, ok, ok, ks, ok, 2, 8, 8, None) == 0   # nothing to add
+    assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, ok, 8, 8, 100, 1, None) == 2        # K % 128
+    assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, ok, 8, 12, 128, 1, None) == 2       # N % 8
+    assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, ok, -1, 8, 128, 1, None) == 1
+    assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, ok, 8, 8, 0, 1, None) == 0          # K = 0, accumulate: no-op
+    assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, _fake(0x10008), 8, 8, 0, 0, None) == 3  # zeroing misaligned D
 
 
 def test_scale_shapes_follow_the_pages_usage_example():

@@ -169,3 +169,32 @@ def test_kgrouped_workload_sampled_rows(G, M, N):
     want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in, rows=rows)
     for g in range(G):
         check_f32(got[g][rows], want[g], f"k-grouped g={g}")
+
+
+# --------------------------------------------------------------------------- dense weight gradient
+@pytest.mark.parametrize("accumulate", [True, False])
+@pytest.mark.parametrize("M,N,K", [(200, 264, 384), (128, 128, 128), (300, 1000, 1024), (1024, 2048, 4096)])
+def test_dense_wgrad_parity(M, N, K, accumulate):
+    # the single-expert weight gradient, accumulating (D += X^T dY) or overwriting (D = X^T dY)
+    c = I.make_kgrouped(I.seed_for(5, M + N + K), 1, M, N, [K])
+    D = dev(c.D_in[0]) if accumulate else torch.full((M, N), float("nan"), device="cuda")
+    dg.dg_wgrad_fp8_nt(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), D, accumulate=accumulate)
+    assert dg.dg_device_status() == 0
+    D_in = c.D_in if accumulate else torch.zeros(1, M, N)
+    want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, [K], D_in)[0]
+    check_f32(D.cpu().numpy(), want, f"dense wgrad accumulate={accumulate}")
+
+
+def test_dense_wgrad_k_zero():
+    M, N = 130, 64
+    D = torch.full((M, N), 3.0, device="cuda")
+    dg.dg_wgrad_fp8_nt(torch.empty(M, 0, dtype=torch.uint8, device="cuda"), torch.empty(M, 0, device="cuda"),
+                       torch.empty(N, 0, dtype=torch.uint8, device="cuda"), torch.empty(N, 0, device="cuda"), D,
+                       accumulate=True)
+    assert dg.dg_device_status() == 0
+    assert bool((D == 3.0).all())          # nothing to add: unchanged
+    dg.dg_wgrad_fp8_nt(torch.empty(M, 0, dtype=torch.uint8, device="cuda"), torch.empty(M, 0, device="cuda"),
+                       torch.empty(N, 0, dtype=torch.uint8, device="cuda"), torch.empty(N, 0, device="cuda"), D,
+                       accumulate=False)
+    assert dg.dg_device_status() == 0
+    assert bool((D == 0.0).all())          # the empty product, stored
