@@ -61,6 +61,17 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
                          void* D, int M, int N, int K, cudaStream_t stream);
 
 /*
+ * The normal GEMM for the other operand layouts (the pages list NT, TN, NN and TT for SM100): the same
+ * product D = A . B^T with the same scales, but A may be stored transposed, [K, M] with M contiguous
+ * (a_mn_major != 0), and B transposed, [K, N] with N contiguous (b_mn_major != 0). sfa stays
+ * [M, K/128] and sfb [ceil(N/128), K/128]. An MN-major operand needs its contiguous extent (M or N)
+ * to be a multiple of 16 (DG_UNSUPPORTED_SHAPE otherwise). dg_gemm_fp8(..., 0, 0, ...) is
+ * dg_gemm_fp8_nt.
+ */
+dg_status dg_gemm_fp8(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
+                      int M, int N, int K, int a_mn_major, int b_mn_major, cudaStream_t stream);
+
+/*
  * m-grouped GEMM, contiguous layout (pages: m_grouped_gemm_fp8_fp8_bf16_nt_contiguous; for training
  * forward and inference prefill). The experts' token rows are stacked along M; each expert's segment
  * starts on a multiple of 128 rows (segments padded to 128).

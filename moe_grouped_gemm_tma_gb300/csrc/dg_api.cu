@@ -87,6 +87,19 @@ dg_status make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int64
     return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
 }
 
+// MN-major e4m3 operand stored [k, cols] (cols contiguous: A as [K, M] or B as [K, N]) read in boxes of
+// 128 columns x 128 k rows with the 128-byte swizzle, the layout of the MN-major MMA descriptors.
+dg_status make_mn_operand_map(CUtensorMap* m, const void* base, int64_t k, int64_t cols) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(k)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {128u, 128u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
+}
+
 // Row-major BF16 output [rows, n] written in boxes of 32 rows x 16 columns (32 bytes) with the
 // 32-byte swizzle the epilogue's staging buffers use.
 dg_status make_output_map(CUtensorMap* m, void* base, int64_t rows, int64_t n) {
@@ -123,6 +136,8 @@ struct Spec {
 };
 constexpr Spec kNormalSpecs1[] = {{64, 1}, {96, 1}, {128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
 constexpr Spec kNormalSpecs2[] = {{128, 2}, {160, 2}, {192, 2}, {224, 2}, {256, 2}};
+// B stored MN-major is staged in whole 128-column boxes
+constexpr Spec kNormalSpecsBMN[] = {{128, 1}, {256, 1}};
 constexpr Spec kContiguousSpecs[] = {{128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
 constexpr Spec kMaskedSpecs1[] = {{64, 1}, {128, 1}, {192, 1}, {256, 1}};
 constexpr Spec kMaskedSpecs2[] = {{128, 2}, {256, 2}};
@@ -329,6 +344,70 @@ static dg_status wgrad_impl(const uint8_t* A, const float* sfa, const uint8_t* B
 }
 
 
+// The normal GEMM for every operand layout: A stored [M, K] or (a_mn) [K, M], B stored [N, K] or
+// (b_mn) [K, N]. MN-major operands need their contiguous extent to be a multiple of 16 (TMA row
+// strides); MN-major B is tiled in whole 128-column boxes; CTA pairs serve the K-major layout only.
+static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
+                           int M, int N, int K, bool a_mn, bool b_mn, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
+    if (M == 0 || N == 0) return DG_OK;
+    if (!D) return DG_INVALID_ARG;
+    if (K % 128 != 0 || N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if ((a_mn && M % 16 != 0) || (b_mn && N % 16 != 0)) return DG_UNSUPPORTED_SHAPE;
+    if (!aligned(D, 16)) return DG_MISALIGNED;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+    if (K == 0)
+        return cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
+
+    const bool pair = !a_mn && !b_mn && use_pair(M);
+    Spec sp;
+    int split = 1;
+    if (b_mn) {
+        sp = spec_override(kNormalSpecsBMN, choose_spec(kNormalSpecsBMN, cdiv(M, BM), N, dev.sms));
+        split = choose_split(kNormalSpecsBMN, &sp, cdiv(M, BM), N, K / 128, dev.sms);
+    } else if (pair) {
+        sp = spec_override(kNormalSpecs2, choose_spec(kNormalSpecs2, cdiv(M, 2 * BM), N, dev.sms));
+    } else {
+        sp = spec_override(kNormalSpecs1, choose_spec(kNormalSpecs1, cdiv(M, BM), N, dev.sms));
+        split = choose_split(kNormalSpecs1, &sp, cdiv(M, BM), N, K / 128, dev.sms);
+    }
+    const int bn = sp.bn;
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if ((a_mn ? make_mn_operand_map(&L.tmap_a, A, K, M) : make_operand_map(&L.tmap_a, A, M, K, BM)) != DG_OK)
+        return DG_CUDA_ERROR;
+    if ((b_mn ? make_mn_operand_map(&L.tmap_b, B, K, N) : make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair)) != DG_OK)
+        return DG_CUDA_ERROR;
+    if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.status = dev.status;
+    p.rows = M;
+    p.n = N;
+    p.kbs = K / 128;
+    p.groups = 1;
+    p.sfb_rows = cdiv(N, 128);
+    p.m_blocks = cdiv(M, BM * sp.pair);
+    p.n_blocks = cdiv(N, bn);
+    p.group_m = choose_group_m(p.m_blocks, BM * sp.pair, K, dev);
+    p.split = split;
+    p.a_mn = a_mn ? 1 : 0;
+    p.b_mn = b_mn ? 1 : 0;
+    const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
+    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = static_cast<int>(tiles);
+    L.units = p.tiles;
+    L.sms = dev.sms;
+    L.stream = stream;
+    return launch_spec<kNormal>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
 extern "C" {
 
 const char* dg_status_string(dg_status s) {
@@ -361,50 +440,12 @@ dg_status dg_device_status(cudaStream_t stream) {
 
 dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
                          int M, int N, int K, cudaStream_t stream) {
-    if (M < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
-    if (M == 0 || N == 0) return DG_OK;
-    if (!D) return DG_INVALID_ARG;
-    if (K % 128 != 0 || N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
-    if (!aligned(D, 16)) return DG_MISALIGNED;
-    DeviceInfo dev;
-    dg_status st = common_prologue(&dev);
-    if (st != DG_OK) return st;
-    if (K == 0)
-        return cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
-    if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
-    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
+    return gemm_impl(A, sfa, B, sfb, D, M, N, K, false, false, stream);
+}
 
-    const bool pair = use_pair(M);
-    Spec sp = pair ? spec_override(kNormalSpecs2, choose_spec(kNormalSpecs2, cdiv(M, 2 * BM), N, dev.sms))
-                   : spec_override(kNormalSpecs1, choose_spec(kNormalSpecs1, cdiv(M, BM), N, dev.sms));
-    const int split = pair ? 1 : choose_split(kNormalSpecs1, &sp, cdiv(M, BM), N, K / 128, dev.sms);
-    const int bn = sp.bn;
-    Launch L;
-    std::memset(&L, 0, sizeof(L));
-    if (make_operand_map(&L.tmap_a, A, M, K, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
-    if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
-    Params& p = L.params;
-    p.sfa = sfa;
-    p.sfb = sfb;
-    p.d = D;
-    p.status = dev.status;
-    p.rows = M;
-    p.n = N;
-    p.kbs = K / 128;
-    p.groups = 1;
-    p.sfb_rows = cdiv(N, 128);
-    p.m_blocks = cdiv(M, BM * sp.pair);
-    p.n_blocks = cdiv(N, bn);
-    p.group_m = choose_group_m(p.m_blocks, BM * sp.pair, K, dev);
-    p.split = split;
-    const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
-    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
-    p.tiles = static_cast<int>(tiles);
-    L.units = p.tiles;
-    L.sms = dev.sms;
-    L.stream = stream;
-    return launch_spec<kNormal>(sp, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+dg_status dg_gemm_fp8(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D, int M,
+                      int N, int K, int a_mn_major, int b_mn_major, cudaStream_t stream) {
+    return gemm_impl(A, sfa, B, sfb, D, M, N, K, a_mn_major != 0, b_mn_major != 0, stream);
 }
 
 dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,

@@ -88,6 +88,7 @@ struct Params {
     int split;                 // normal layout, single-CTA tiles: CTAs (a cluster) sharing one tile's K
     int group_m;               // normal / contiguous: row blocks per raster band (row block fastest)
     int overwrite;             // k-grouped: store the tile (D = ...) instead of adding it (D += ...)
+    int a_mn, b_mn;            // normal layout: A stored [K, M] / B stored [K, N] (MN-major operands)
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
@@ -446,8 +447,16 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         if (PAIR == 1 || leader) {
                             if (issuer) {
                                 mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
-                                tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
-                                tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                                // MN-major operands: boxes of 128 M (N) bytes x 128 k rows; B takes one
+                                // box per 128 columns of the tile (the host allows it for BN % 128 == 0)
+                                if ((MODE == kNormal && p.a_mn)) tma_load_2d(&tmap_a, &full_bar[stage], a_dst, ti.a_row, x);
+                                else tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
+                                if ((MODE == kNormal && p.b_mn)) {
+                                    for (int j = 0; j < C::B_ROWS / 128; ++j)
+                                        tma_load_2d(&tmap_b, &full_bar[stage], b_dst + j * (128 * BK), ti.b_row + 128 * j, x);
+                                } else {
+                                    tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
+                                }
                             }
                         } else {
                             const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
@@ -513,17 +522,21 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     tc_fence_after();
                     for (int j = 0; j < take; ++j) {
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                        const uint64_t a_desc = sw128_kmajor_desc(a_base + stage * C::A_BYTES);
-                        const uint64_t b_desc = sw128_kmajor_desc(b_base + stage * C::B_BYTES);
+                        const uint32_t a_addr = a_base + stage * C::A_BYTES, b_addr = b_base + stage * C::B_BYTES;
+                        const uint64_t a_desc = (MODE == kNormal && p.a_mn) ? sw128_mnmajor_desc(a_addr, 128 * BK) : sw128_kmajor_desc(a_addr);
+                        const uint64_t b_desc = (MODE == kNormal && p.b_mn) ? sw128_mnmajor_desc(b_addr, 128 * BK) : sw128_kmajor_desc(b_addr);
+                        // K-major: K = 32 is 32 bytes along the swizzled row (>> 4 = 2); MN-major: 32 rows
+                        // of k, four whole 1024-byte atoms (>> 4 = 256)
+                        const uint32_t a_kstep = (MODE == kNormal && p.a_mn) ? (32 * 128) >> 4 : UMMA_K >> 4;
+                        const uint32_t b_kstep = (MODE == kNormal && p.b_mn) ? (32 * 128) >> 4 : UMMA_K >> 4;
+                        const uint32_t idesc = IDESC | ((MODE == kNormal && p.a_mn) ? IDESC_A_MN : 0u) | ((MODE == kNormal && p.b_mn) ? IDESC_B_MN : 0u);
                         if (issuer) {
 #pragma unroll
                             for (int k = 0; k < BK / UMMA_K; ++k) {
-                                // advancing the start address by 32 bytes (>> 4 = 2) steps K by 32 within
-                                // the 128-byte swizzle row
-                                const uint64_t ad = a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
-                                const uint64_t bd = b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
-                                if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
-                                else mma_f8f6f4(d_tmem, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                                const uint64_t ad = a_desc + static_cast<uint64_t>(k * a_kstep);
+                                const uint64_t bd = b_desc + static_cast<uint64_t>(k * b_kstep);
+                                if (PAIR == 2) mma_f8f6f4_pair(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+                                else mma_f8f6f4(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
                             }
                             if (PAIR == 2) {
                                 mma_commit_pair(&empty_bar[stage], 0x3);

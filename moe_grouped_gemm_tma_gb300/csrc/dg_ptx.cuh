@@ -190,13 +190,29 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile (the matrix stored with M or N
+// contiguous) written by TMA with the 128-byte swizzle: rows of 128 bytes hold 128 consecutive M (N)
+// values of one k, 8-row (1024-byte) swizzle atoms follow each other along K, and further 128-wide
+// column blocks of the tile follow at `mn_stride` bytes.
+//   bits 16-29 leading byte offset >> 4 = mn_stride (next 128 M/N values)
+//   bits 32-45 stride byte offset >> 4 = 1024 (next 8 values of K)
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t mn_stride) {
+    return static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B, FP32 accumulator, both K-major, MxN.
 //   bits 4-5 D format (1 = F32)   bits 7-9 A format (0 = E4M3)   bits 10-12 B format (0 = E4M3)
-//   bit 15/16 A/B major (0 = K)   bits 17-22 N >> 3             bits 24-28 M >> 4
+//   bit 15/16 A/B major (0 = K, 1 = MN; see IDESC_A_MN / IDESC_B_MN)
+//   bits 17-22 N >> 3             bits 24-28 M >> 4
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
     return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
 }
+
+constexpr uint32_t IDESC_A_MN = 1u << 15;
+constexpr uint32_t IDESC_B_MN = 1u << 16;
 
 // D[tmem] (+)= A[smem] . B[smem]^T for one M x N x 32 block, issued by one thread.
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

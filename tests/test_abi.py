@@ -55,6 +55,9 @@ def test_rejects_bad_shapes_before_any_cuda_call():
     assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, ok, 4, 12, 128, None) == 2         # N % 8
     assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, _fake(0x10008), 4, 8, 128, None) == 3  # D misaligned
     assert L.dg_gemm_fp8_nt(ok, ok, ok, ok, None, 4, 8, 128, None) == 1
+    assert L.dg_gemm_fp8(ok, ok, ok, ok, ok, 24, 16, 128, 1, 0, None) == 2     # A stored [K, M], M % 16
+    assert L.dg_gemm_fp8(ok, ok, ok, ok, ok, 16, 24, 128, 0, 1, None) == 2     # B stored [K, N], N % 16
+    assert L.dg_gemm_fp8(ok, ok, ok, ok, ok, 0, 16, 128, 1, 1, None) == 0      # empty: no-op
     assert L.dg_m_grouped_contiguous(ok, ok, ok, ok, ok, ok, 100, 8, 128, 2, None) == 2  # Mt % 128
     assert L.dg_m_grouped_contiguous(ok, ok, ok, ok, ok, ok, 128, 8, 128, 0, None) == 1  # G = 0
     assert L.dg_m_grouped_masked(ok, ok, ok, ok, ok, ok, 2000, 64, 8, 128, 0, None) == 1  # G too large
