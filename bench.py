@@ -12,6 +12,7 @@ Workloads (--workload; one "step" = every case of the workload once, each on its
   (512, 128), (1024, 256)}, masked_m U[0.7, 1.0] x expected_m, (N, K) as above.
 * kgrouped: k-grouped FP32 weight gradient, G in {4, 8}, tokens per expert U[0.5, 1.5] x 4096 padded
   to 128, (M, N) in {(7168, 4096), (2048, 7168)}.
+* layouts: the M=4096 dense GEMMs with A and/or B stored transposed (TN, NN, TT).
 
 Inputs are seeded synthetic N(0,1) values block-quantised to e4m3 (drawn on the GPU with the same
 counter-based generator the tests use on the CPU). Every case has its own buffers, so the working set of
@@ -56,6 +57,8 @@ WORKLOADS = {
                    "U[0.7,1.3] x {8192,4096} padded to 128, (N,K) in {(4096,7168),(7168,2048)}, BF16 out"),
     "masked": ("m-grouped masked FP8 GEMM (MoE decode), G in {1,2,4,16}, (max_m, expected_m) in {(256,64),"
                "(512,128),(1024,256)}, masked_m U[0.7,1.0] x expected_m, (N,K) in {(4096,7168),(7168,2048)}"),
+    "layouts": ("dense normal FP8 GEMM, M=4096, (N,K) as the dense workload, with transposed operand storage: "
+                "TN (A stored [K,M]), NN (B stored [K,N]), TT (both); BF16 out"),
     "kgrouped": ("k-grouped FP8 weight-gradient GEMM, FP32 accumulated, G in {4,8}, tokens per expert "
                  "U[0.5,1.5] x 4096 padded to 128, (M,N) in {(7168,4096),(2048,7168)}"),
 }
@@ -196,6 +199,31 @@ def dense_cases(only=None):
     return cases
 
 
+def layouts_cases():
+    """The M=4096 dense GEMMs with transposed operand storage: TN (A stored [K, M]), NN (B stored
+    [K, N]) and TT (both)."""
+    import moe_grouped_gemm_tma_gb300 as dg
+    from moe_grouped_gemm_tma_gb300 import inputs as I
+    from oracle import oracle as O
+    M = 4096
+    cases = []
+    for (N, K) in NKS:
+        c = I.make_normal(I.seed_for(1, 0), M, N, K)
+        kb, nb = K // 128, (N + 127) // 128
+        for name, a_mn, b_mn in (("TN", True, False), ("NN", False, True), ("TT", True, True)):
+            inp = {"A": c.A.t().contiguous() if a_mn else c.A, "sfa": c.sfa,
+                   "B": c.B.t().contiguous() if b_mn else c.B, "sfb": c.sfb}
+            cases.append(Case(
+                f"{name} {M}x{N}x{K}", 2.0 * M * N * K, M * K + N * K + 4 * M * kb + 4 * nb * kb + 2 * M * N, inp,
+                (M, N), torch.bfloat16,
+                (lambda a, b: lambda d, o, s: dg.dg_gemm_fp8(d["A"], d["sfa"], d["B"], d["sfb"], o, a_mn_major=a,
+                                                              b_mn_major=b, stream=s))(a_mn, b_mn),
+                (lambda a, b: lambda h, r: (O.gemm_fp8_nt((h["A"].t() if a else h["A"])[:r].contiguous(), h["sfa"][:r],
+                                                          (h["B"].t() if b else h["B"]).contiguous(), h["sfb"]),
+                                            2.0 * r * N * K)[1])(a_mn, b_mn)))
+    return cases
+
+
 def contiguous_cases():
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
@@ -272,7 +300,8 @@ def build_cases(workload, shape=None, only=None):
     if workload == "dense":
         cases = dense_cases(shape)
     else:
-        cases = {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases}[workload]()
+        cases = {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases,
+                 "layouts": layouts_cases}[workload]()
     if only:
         cases = [c for c in cases if only in c.name]
         if not cases:
