@@ -46,7 +46,8 @@ enum {
     DG_MISALIGNED = 3,         /* a pointer not aligned as stated above */
     DG_CUDA_ERROR = 4,         /* a CUDA runtime/driver call or launch failed */
     DG_NO_DEVICE_SUPPORT = 5,  /* current device is not compute capability 10.3 */
-    DG_DEVICE_TIMEOUT = 6      /* a kernel's bounded wait expired (reported by dg_device_status) */
+    DG_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait expired (reported by dg_device_status) */
+    DG_SCALE_NOT_UE8M0 = 7     /* a UE8M0-path scale was not a power of two (reported by dg_device_status) */
 };
 
 /*
@@ -70,6 +71,16 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
  */
 dg_status dg_gemm_fp8(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
                       int M, int N, int K, int a_mn_major, int b_mn_major, cudaStream_t stream);
+
+/*
+ * The normal GEMM for power-of-two scales, on the block-scaled tensor-core path (pages: the SM100
+ * UE8M0 scale format): same arguments and result as dg_gemm_fp8_nt, but every sfa and sfb entry must
+ * be a positive power of two in [2^-126, 2^127]. The tensor core applies the scales as 8-bit exponents
+ * while it accumulates, so no per-128-K promotion runs. A scale that is not a power of two is
+ * reported by dg_device_status as DG_SCALE_NOT_UE8M0 (its result is then unspecified).
+ */
+dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
+                               int M, int N, int K, cudaStream_t stream);
 
 /*
  * m-grouped GEMM, contiguous layout (pages: m_grouped_gemm_fp8_fp8_bf16_nt_contiguous; for training
@@ -133,8 +144,8 @@ const char* dg_status_string(dg_status status);
 
 /*
  * Synchronises `stream`, then reports (and clears) a device-side timeout recorded by any dg kernel
- * on the current device since the last call: DG_DEVICE_TIMEOUT, else DG_CUDA_ERROR if the
- * synchronisation failed, else DG_OK.
+ * on the current device since the last call: DG_DEVICE_TIMEOUT, or DG_SCALE_NOT_UE8M0 from the UE8M0
+ * path, else DG_CUDA_ERROR if the synchronisation failed, else DG_OK.
  */
 dg_status dg_device_status(cudaStream_t stream);
 

@@ -17,7 +17,7 @@ import os
 import threading
 
 __all__ = [
-    "DGError", "load", "dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
+    "DGError", "load", "dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
     "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status", "dg_status_string", "scale_shapes", "library_path",
 ]
 
@@ -26,7 +26,7 @@ _lib = None
 
 DG_OK = 0
 STATUS_NAMES = {0: "DG_OK", 1: "DG_INVALID_ARG", 2: "DG_UNSUPPORTED_SHAPE", 3: "DG_MISALIGNED",
-                4: "DG_CUDA_ERROR", 5: "DG_NO_DEVICE_SUPPORT", 6: "DG_DEVICE_TIMEOUT"}
+                4: "DG_CUDA_ERROR", 5: "DG_NO_DEVICE_SUPPORT", 6: "DG_DEVICE_TIMEOUT", 7: "DG_SCALE_NOT_UE8M0"}
 
 
 class DGError(RuntimeError):
@@ -53,6 +53,7 @@ def load(build_if_missing: bool = True):
             P, I = ctypes.c_void_p, ctypes.c_int
             L.dg_gemm_fp8_nt.argtypes = [P, P, P, P, P, I, I, I, P]
             L.dg_gemm_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+            L.dg_gemm_fp8_nt_ue8m0.argtypes = [P, P, P, P, P, I, I, I, P]
             L.dg_m_grouped_contiguous.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
             L.dg_m_grouped_masked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
             L.dg_k_grouped_wgrad.argtypes = [P, P, P, P, P, P, I, I, I, P]
@@ -60,7 +61,7 @@ def load(build_if_missing: bool = True):
             L.dg_device_status.argtypes = [P]
             L.dg_status_string.argtypes = [I]
             L.dg_status_string.restype = ctypes.c_char_p
-            for f in ("dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
+            for f in ("dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
                       "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status"):
                 getattr(L, f).restype = I
             _lib = L
@@ -154,6 +155,25 @@ def dg_gemm_fp8(A, sfa, B, sfb, D, a_mn_major=False, b_mn_major=False, stream=No
     st = load().dg_gemm_fp8(_ptr(A), _ptr(sfa), _ptr(B), _ptr(sfb), _ptr(D), M, N, K,
                             1 if a_mn_major else 0, 1 if b_mn_major else 0, _stream(stream))
     _check(st, "dg_gemm_fp8")
+    return D
+
+
+def dg_gemm_fp8_nt_ue8m0(A, sfa, B, sfb, D, stream=None):
+    """dg_gemm_fp8_nt for power-of-two scales on the block-scaled (UE8M0) tensor-core path."""
+    torch = _torch()
+    A, B = _codes(A, "A"), _codes(B, "B")
+    sfa, sfb = _f32(sfa, "sfa"), _f32(sfb, "sfb")
+    D = _dense(D, "D")
+    if D.dtype != torch.bfloat16:
+        raise TypeError("D must be bfloat16")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)} B {tuple(B.shape)} D {tuple(D.shape)}")
+    if (tuple(sfa.shape), tuple(sfb.shape)) != scale_shapes(M, N, K):
+        raise ValueError(f"scale shapes {tuple(sfa.shape)}, {tuple(sfb.shape)} != {scale_shapes(M, N, K)}")
+    st = load().dg_gemm_fp8_nt_ue8m0(_ptr(A), _ptr(sfa), _ptr(B), _ptr(sfb), _ptr(D), M, N, K, _stream(stream))
+    _check(st, "dg_gemm_fp8_nt_ue8m0")
     return D
 
 

@@ -136,6 +136,8 @@ struct Spec {
 };
 constexpr Spec kNormalSpecs1[] = {{64, 1}, {96, 1}, {128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
 constexpr Spec kNormalSpecs2[] = {{128, 2}, {160, 2}, {192, 2}, {224, 2}, {256, 2}};
+// block-scaled (UE8M0) normal GEMM
+constexpr Spec kBlockScaledSpecs[] = {{128, 1}, {192, 1}, {224, 1}, {256, 1}};
 // B stored MN-major is staged in whole 128-column boxes
 constexpr Spec kNormalSpecsBMN[] = {{128, 1}, {256, 1}};
 constexpr Spec kContiguousSpecs[] = {{128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
@@ -419,6 +421,7 @@ const char* dg_status_string(dg_status s) {
         case DG_CUDA_ERROR: return "DG_CUDA_ERROR";
         case DG_NO_DEVICE_SUPPORT: return "DG_NO_DEVICE_SUPPORT";
         case DG_DEVICE_TIMEOUT: return "DG_DEVICE_TIMEOUT";
+        case DG_SCALE_NOT_UE8M0: return "DG_SCALE_NOT_UE8M0";
     }
     return "DG_UNKNOWN_STATUS";
 }
@@ -433,7 +436,7 @@ dg_status dg_device_status(cudaStream_t stream) {
     if (v != 0) {
         const int zero = 0;
         if (cudaMemcpy(dev.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DG_CUDA_ERROR;
-        return DG_DEVICE_TIMEOUT;
+        return v == DG_SCALE_NOT_UE8M0 ? DG_SCALE_NOT_UE8M0 : DG_DEVICE_TIMEOUT;
     }
     return DG_OK;
 }
@@ -446,6 +449,58 @@ dg_status dg_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, c
 dg_status dg_gemm_fp8(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D, int M,
                       int N, int K, int a_mn_major, int b_mn_major, cudaStream_t stream) {
     return gemm_impl(A, sfa, B, sfb, D, M, N, K, a_mn_major != 0, b_mn_major != 0, stream);
+}
+
+dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
+                               int M, int N, int K, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
+    if (M == 0 || N == 0) return DG_OK;
+    if (!D) return DG_INVALID_ARG;
+    if (K % 128 != 0 || N % 8 != 0) return DG_UNSUPPORTED_SHAPE;
+    if (!aligned(D, 16)) return DG_MISALIGNED;
+    DeviceInfo dev;
+    dg_status st = common_prologue(&dev);
+    if (st != DG_OK) return st;
+    if (K == 0)
+        return cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
+
+    const Spec sp = spec_override(kBlockScaledSpecs, choose_spec(kBlockScaledSpecs, cdiv(M, BM), N, dev.sms));
+    const int bn = sp.bn;
+    Launch L;
+    std::memset(&L, 0, sizeof(L));
+    if (make_operand_map(&L.tmap_a, A, M, K, BM) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
+    Params& p = L.params;
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.d = D;
+    p.status = dev.status;
+    p.rows = M;
+    p.n = N;
+    p.kbs = K / 128;
+    p.groups = 1;
+    p.sfb_rows = cdiv(N, 128);
+    p.m_blocks = cdiv(M, BM);
+    p.n_blocks = cdiv(N, bn);
+    p.group_m = choose_group_m(p.m_blocks, BM, K, dev);
+    p.split = 1;
+    const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
+    if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+    p.tiles = static_cast<int>(tiles);
+    L.units = p.tiles;
+    L.sms = dev.sms;
+    L.stream = stream;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (bn) {
+        case 128: e = launch_bs<128>(L); break;
+        case 192: e = launch_bs<192>(L); break;
+        case 224: e = launch_bs<224>(L); break;
+        case 256: e = launch_bs<256>(L); break;
+    }
+    return e == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
 }
 
 dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,

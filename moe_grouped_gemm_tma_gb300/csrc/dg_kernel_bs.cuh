@@ -1,0 +1,316 @@
+// Block-scaled variant of the normal GEMM for power-of-two scales, for sm_103a.
+//
+// Same product as dg_gemm_kernel in the normal layout,
+//   D[m,n] = sum_kb sfa[m,kb] * sfb[n/128,kb] * sum_{k in block kb} A[m,k] B[n,k],
+// but when every scale is a power of two the scaling can be done by the tensor core itself:
+// tcgen05.mma.kind::mxf8f6f4.block_scale multiplies each 32-element slice of A's row m and B's row n by
+// an 8-bit exponent (UE8M0) read from TMEM while it accumulates, so the whole K of a tile accumulates in
+// one TMEM accumulator and nothing is promoted per K block (the pages' "UE8M0 block-scaled path" for
+// SM100; the 1x128 and 128x128 FP32 scales become the same exponent for all four 32-element slices of a
+// 128-K block).
+//
+// Warp roles (384 threads; no register re-split, no role holds large state):
+//   warp 0      TMA producer: A and B tiles of every K block into a STAGES-deep ring.
+//   warp 1      TMEM owner and MMA issuer: per K block four block-scaled MMAs (K = 32, scale bytes 0..3)
+//               into the tile's accumulator, then commits the stage and the scale slot; at the end of a
+//               tile commits the accumulator.
+//   warps 4..7  scale writers (one per TMEM lane quarter): per K block they turn the FP32 scales into
+//               exponents and store them with tcgen05.st into a TMEM scale slot: A's row m (lane m) in
+//               four columns (the MMA reads row m's from column m / 32), B's row n (replicated in every
+//               lane quarter, lane n % 32) in column n / 32 after them. A scale that is not a power of two
+//               is reported (DG_SCALE_NOT_UE8M0).
+//   warps 8..11 output: per tile they read the accumulator out of TMEM, release it, round to BF16 and
+//               TMA-store 32 x 16 boxes.
+// Every wait is bounded as in dg_gemm_kernel.
+#pragma once
+
+#include "dg_kernel.cuh"
+
+namespace dg {
+
+constexpr int STATUS_SCALE_NOT_UE8M0 = 7;   // DG_SCALE_NOT_UE8M0
+
+template <int BN>
+struct CfgBS {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int OUT_WARPS = 4;
+    static constexpr int STORE_BYTES = OUT_WARPS * 2048;
+    static constexpr int STATIC_RESERVE = 640;
+    static constexpr int STAGES = ring_stages(STAGE_BYTES, 0, STORE_BYTES, STATIC_RESERVE);
+    // TMEM: NACC accumulators of BN columns, then scale slots of 16 columns (A: 4, B: from +8, one per
+    // 32 rows of B, at most 8)
+    static constexpr int SLOT_COLS = 16;
+    static constexpr int SFB_OFF = 8;
+    static constexpr int NACC = (2 * BN + 2 * SLOT_COLS <= TMEM_COLS) ? 2 : 1;
+    static constexpr int SF_COL0 = NACC * BN;
+    static constexpr int SLOTS_FIT = (TMEM_COLS - SF_COL0) / SLOT_COLS;
+    static constexpr int SLOTS = SLOTS_FIT > 8 ? 8 : SLOTS_FIT;
+    static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + 1023) / 1024) * 1024;
+    static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
+    static_assert(SLOTS >= 2, "at least two scale slots");
+    static_assert(STAGES >= 2, "not enough shared memory for two stages");
+    static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte swizzle-atom alignment");
+};
+
+// Exponent byte of a power-of-two FP32 scale, replicated into the four bytes of a TMEM cell (one per
+// 32-element slice of the 128-K block); anything else is reported and its exponent used.
+__device__ __forceinline__ uint32_t ue8m0x4(float s, int* status) {
+    const uint32_t bits = __float_as_uint(s);
+    if ((bits & 0x807FFFFFu) != 0u || bits == 0u) atomicExch(status, STATUS_SCALE_NOT_UE8M0);
+    return ((bits >> 23) & 0xFFu) * 0x01010101u;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                  const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ Params p) {
+    using C = CfgBS<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int NACC = C::NACC;
+    constexpr int SLOTS = C::SLOTS;
+    constexpr uint32_t IDESC = idesc_bs_e4m3(BM, BN);
+
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
+    __shared__ uint64_t tmem_full_bar[NACC], tmem_empty_bar[NACC];
+    __shared__ uint64_t sf_full_bar[SLOTS], sf_empty_bar[SLOTS];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = static_cast<int>(blockIdx.x);
+    const int num_units = static_cast<int>(gridDim.x);
+    const uint32_t raw = smem_u32(dyn_smem);
+    uint8_t* smem = dyn_smem + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* smem_a = smem;
+    uint8_t* smem_b = smem + STAGES * C::A_BYTES;
+    uint8_t* s_store = smem + C::STORE_OFF;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int a = 0; a < NACC; ++a) {
+            mbar_init(&tmem_full_bar[a], 1);
+            mbar_init(&tmem_empty_bar[a], C::OUT_WARPS);
+        }
+        for (int s = 0; s < SLOTS; ++s) {
+            mbar_init(&sf_full_bar[s], 4);
+            mbar_init(&sf_empty_bar[s], 1);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&s_tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = s_tmem_base;
+    volatile int* abort_flag = &s_abort;
+    const int num_tiles = p.tiles;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------------- TMA producer
+        const bool issuer = elect_one();
+        if (issuer) {
+            prefetch_tmap(&tmap_a);
+            prefetch_tmap(&tmap_b);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_parity = 0;
+        bool ok = true;
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                if (issuer) {
+                    const int x = (ti.kb0 + kb) * BK;
+                    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+                    tma_load_2d(&tmap_a, &full_bar[stage], smem_a + stage * C::A_BYTES, x, ti.a_row);
+                    tma_load_2d(&tmap_b, &full_bar[stage], smem_b + stage * C::B_BYTES, x, ti.b_row);
+                }
+                __syncwarp();
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (ok) {
+            // every stage this CTA filled has been consumed before the CTA may exit
+            for (int i = 0; i < STAGES && ok; ++i) {
+                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, got)) ok = false;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok && issuer) {
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s)) drain_wait(&full_bar[s], (issued_parity >> s) & 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------------- MMA issuer
+        const bool issuer = elect_one();
+        int stage = 0, slot = 0, acc = 0;
+        uint32_t phase = 0, sphase = 0, aphase = 0;
+        bool ok = true, any = false;
+        int last_acc = 0;
+        uint32_t last_parity = 0;
+        const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            // the tile's accumulator must have been read out by the output warps
+            const bool free_acc = wait_bounded(&tmem_empty_bar[acc], aphase ^ 1u, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, free_acc)) { ok = false; break; }
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                bool got = (static_cast<unsigned>(mbar_try_wait(&full_bar[stage], phase)) &
+                            static_cast<unsigned>(mbar_try_wait(&sf_full_bar[slot], sphase))) != 0u;
+                if (!got)
+                    got = wait_bounded(&full_bar[stage], phase, abort_flag, p.status) &&
+                          wait_bounded(&sf_full_bar[slot], sphase, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t a_desc = sw128_kmajor_desc(a_base + stage * C::A_BYTES);
+                const uint64_t b_desc = sw128_kmajor_desc(b_base + stage * C::B_BYTES);
+                const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
+                const uint32_t sfb_t = sfa_t + C::SFB_OFF;
+                if (issuer) {
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // 32-element slice k of the block: scale byte k of every cell
+                        mma_f8f6f4_bs(d_tmem, a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4)),
+                                      b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4)),
+                                      IDESC | IDESC_BS_SFA(k) | IDESC_BS_SFB(k), sfa_t, sfb_t,
+                                      (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty_bar[stage]);
+                    mma_commit(&sf_empty_bar[slot]);
+                }
+                __syncwarp();
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++slot == SLOTS) { slot = 0; sphase ^= 1u; }
+            }
+            if (!ok) break;
+            if (issuer) mma_commit(&tmem_full_bar[acc]);
+            __syncwarp();
+            any = true;
+            last_acc = acc;
+            last_parity = aphase;
+            if (++acc == NACC) { acc = 0; aphase ^= 1u; }
+        }
+        if (!ok && any && issuer) drain_wait(&tmem_full_bar[last_acc], last_parity);
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------------- scale writers
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        int slot = 0;
+        uint32_t sphase = 0;
+        bool ok = true;
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const float* sfa_row = p.sfa + static_cast<size_t>(min(ti.m0 + q * 32 + lane, p.rows - 1)) * p.kbs + ti.kb0;
+            // B scale rows of this lane's columns n0 + 32 j + lane (j < 8; columns past N reuse the last)
+            const float* sfb_rows[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                sfb_rows[j] = p.sfb + static_cast<size_t>(min(ti.n0 + 32 * j + lane, p.n - 1) / 128) * p.kbs + ti.kb0;
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                const bool got = wait_bounded(&sf_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                const uint32_t va = ue8m0x4(sfa_row[kb], p.status);
+                uint32_t vb[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(sfb_rows[j][kb], p.status) : 0u;
+                const uint32_t col = static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
+                tmem_st_x4(lane_base + col, va, va, va, va);
+                tmem_st_x8(lane_base + col + C::SFB_OFF, vb);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full_bar[slot]);
+                if (++slot == SLOTS) { slot = 0; sphase ^= 1u; }
+            }
+        }
+    } else if (warp >= 8) {
+        // ---------------------------------------------------------------------- output
+        const int q = warp & 3;
+        const int ow = warp - 8;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        int acc = 0;
+        uint32_t aphase = 0, store_round = 0;
+        uint8_t* wbuf = s_store + ow * 2048;
+        const int sw = (lane >> 2) & 1;
+        for (int t = unit; t < num_tiles; t += num_units) {
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const bool got = wait_bounded(&tmem_full_bar[acc], aphase, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            const uint32_t taddr = lane_base + static_cast<uint32_t>(acc * BN);
+            const int y = ti.m0 + q * 32;
+            constexpr int CH = BN / 16;
+            // loads of chunk c + 1 are in flight while chunk c is rounded and staged
+            uint32_t rb[2][16];
+            tmem_ld_x16(taddr, rb[0]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int b = c & 1;
+                if (c + 1 < CH) {
+                    tmem_ld_x16(taddr + (c + 1) * 16, rb[b ^ 1]);
+                } else {
+                    // every load of the accumulator has completed: release it to the next tile's MMAs
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tmem_empty_bar[acc]);
+                }
+                uint8_t* half = wbuf + (store_round & 1u) * 1024;
+                ++store_round;
+                if (lane == 0) bulk_wait_read_1();
+                __syncwarp();
+                const uint32_t* r = rb[b];
+                uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
+                rowp[sw] = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                      pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                      pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                      pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+                rowp[sw ^ 1] = make_uint4(pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                          pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                          pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                          pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmap_d, half, ti.n0 + c * 16, y);
+                    bulk_commit();
+                }
+                if (c + 1 < CH) tmem_ld_wait();
+            }
+            if (++acc == NACC) { acc = 0; aphase ^= 1u; }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace dg

@@ -24,6 +24,10 @@ struct Launch {
 template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L);
 
+// The block-scaled (UE8M0) normal GEMM (dg_inst_bs.cu).
+template <int BN>
+cudaError_t launch_bs(const Launch& L);
+
 // Programmatic dependent launch is on unless DG_PDL=0.
 inline bool pdl_enabled() {
     static const bool on = [] {

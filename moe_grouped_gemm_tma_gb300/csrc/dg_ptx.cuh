@@ -232,6 +232,30 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// Block-scaled MMA (kind::mxf8f6f4.block_scale, one UE8M0 scale per 32 K elements): D[tmem] (+)=
+// (A . diag-scaled) x (B ...) for one M x N x 32 block. The scales are read from TMEM: those of A row
+// m from lane m, column sfa_tmem + m / 32; those of B row n from lane (32 * (m / 32) + n % 32), column
+// sfb_tmem + n / 32 (each lane quarter holds a copy); the byte of each 32-bit cell is chosen by the
+// instruction descriptor (bits 29-30 for A, 4-5 for B). Bit 23 of the descriptor selects UE8M0.
+__device__ __forceinline__ void mma_f8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 block-scaled with E4M3 A and B and UE8M0 scales, MxN; the
+// scale byte indices are OR-ed in per MMA (IDESC_BS_SFA(j) | IDESC_BS_SFB(j)).
+__host__ __device__ constexpr uint32_t idesc_bs_e4m3(int m, int n) {
+    return (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t IDESC_BS_SFA(int j) { return static_cast<uint32_t>(j) << 29; }
+__host__ __device__ constexpr uint32_t IDESC_BS_SFB(int j) { return static_cast<uint32_t>(j) << 4; }
+
 // 32 lanes x 16 consecutive 32-bit columns: thread t of the warp receives lane (base lane + t).
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -241,6 +265,21 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+
+// 32 lanes x N consecutive 32-bit columns from registers: thread t of the warp writes lane (base lane
+// + t); the warp may only address its own lane quarter.
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(taddr), "r"(v0), "r"(v1), "r"(v2), "r"(v3) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

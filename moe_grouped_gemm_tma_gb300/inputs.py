@@ -130,19 +130,29 @@ def _to_e4m3_bytes(x: torch.Tensor) -> torch.Tensor:
     return x.to(torch.float8_e4m3fn).view(torch.uint8)
 
 
-def quantize_1x128(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """Per 1x128 row-block cast of ``x`` [R, K] (K % 128 == 0) -> (uint8 [R, K], fp32 [R, K/128])."""
+def _pow2_at_least(v: torch.Tensor) -> torch.Tensor:
+    """The power of two 2^e with v <= 2^e (frexp: v = m * 2^e, 0.5 <= m < 1)."""
+    _, e = torch.frexp(v)
+    return torch.ldexp(torch.ones_like(v), e)
+
+
+def quantize_1x128(x: torch.Tensor, pow2: bool = False) -> tuple[torch.Tensor, torch.Tensor]:
+    """Per 1x128 row-block cast of ``x`` [R, K] (K % 128 == 0) -> (uint8 [R, K], fp32 [R, K/128]).
+    With ``pow2`` the scale is rounded up to a power of two (UE8M0-representable scales)."""
     R, K = x.shape
     assert K % BLOCK == 0
     xb = x.reshape(R, K // BLOCK, BLOCK)
     amax = xb.abs().amax(dim=2).clamp_min(SCALE_FLOOR)
     s = (amax / E4M3_MAX).to(torch.float32)
+    if pow2:
+        s = _pow2_at_least(s)
     q = _to_e4m3_bytes(xb / s.unsqueeze(2)).reshape(R, K)
     return q.contiguous(), s.contiguous()
 
 
-def quantize_128x128(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """Per 128x128 block cast of ``x`` [N, K] -> (uint8 [N, K], fp32 [ceil(N/128), K/128])."""
+def quantize_128x128(x: torch.Tensor, pow2: bool = False) -> tuple[torch.Tensor, torch.Tensor]:
+    """Per 128x128 block cast of ``x`` [N, K] -> (uint8 [N, K], fp32 [ceil(N/128), K/128]); ``pow2`` as
+    for quantize_1x128."""
     N, K = x.shape
     assert K % BLOCK == 0
     nb = (N + BLOCK - 1) // BLOCK
@@ -151,6 +161,8 @@ def quantize_128x128(x: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
     xb = xp.reshape(nb, BLOCK, K // BLOCK, BLOCK)
     amax = xb.abs().amax(dim=(1, 3)).clamp_min(SCALE_FLOOR)
     s = (amax / E4M3_MAX).to(torch.float32)
+    if pow2:
+        s = _pow2_at_least(s)
     q = _to_e4m3_bytes(xb / s[:, None, :, None]).reshape(nb * BLOCK, K)[:N]
     return q.contiguous(), s.contiguous()
 
@@ -189,9 +201,9 @@ class NormalCase:
     sfb: torch.Tensor    # fp32 [ceil(N/128), K/128]
 
 
-def make_normal(seed: int, M: int, N: int, K: int) -> NormalCase:
-    A, sfa = quantize_1x128(_normal_matrix(seed, STREAM_A, M, K))
-    B, sfb = quantize_128x128(_normal_matrix(seed, STREAM_B, N, K))
+def make_normal(seed: int, M: int, N: int, K: int, pow2: bool = False) -> NormalCase:
+    A, sfa = quantize_1x128(_normal_matrix(seed, STREAM_A, M, K), pow2)
+    B, sfb = quantize_128x128(_normal_matrix(seed, STREAM_B, N, K), pow2)
     return NormalCase(M, N, K, A, sfa, B, sfb)
 
 

@@ -1,0 +1,55 @@
+"""The block-scaled (UE8M0) normal GEMM for power-of-two scales, through the C ABI: compared with the
+oracle of the same product, bitwise on integer-exact inputs, and the report of a scale that is not a
+power of two."""
+import numpy as np
+import pytest
+import torch
+
+import moe_grouped_gemm_tma_gb300 as dg
+from moe_grouped_gemm_tma_gb300 import inputs as I
+from oracle import oracle as O
+from tests.gpu_util import bf16_bits, check_bf16, dev, sentinel_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def run_ue8m0(A, sfa, B, sfb, M, N):
+    D = sentinel_bf16(M, N)
+    dg.dg_gemm_fp8_nt_ue8m0(dev(A), dev(sfa), dev(B), dev(sfb), D)
+    return D
+
+
+@pytest.mark.parametrize("bn", [0, 128, 192, 224, 256])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (200, 1000, 768), (1, 2112, 1024), (520, 4096, 2048)])
+def test_ue8m0_parity(M, N, K, bn, monkeypatch):
+    # power-of-two block scales (amax/448 rounded up to a power of two); ragged M and N; every tile width
+    if bn:
+        monkeypatch.setenv("DG_BN", str(bn))
+    c = I.make_normal(I.seed_for(7, M + N + K), M, N, K, pow2=True)
+    assert bool((torch.frexp(c.sfa)[0] == 0.5).all()) and bool((torch.frexp(c.sfb)[0] == 0.5).all())
+    D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
+    assert dg.dg_device_status() == 0
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 BN={bn} {M}x{N}x{K}")
+
+
+def test_ue8m0_integer_exact_bitwise():
+    # values in {-1, 0, 1} and power-of-two scales 2^-2 .. 2^2 per block: every 32-element slice sums
+    # exactly, every output is a multiple of 2^-4 below 2^13, so the FP32 accumulation is exact and the
+    # only rounding is the final one to BF16, which the oracle takes from the exact value too
+    rng = np.random.default_rng(13)
+    M, N, K = 256, 384, 512
+    codes = np.array([0xB8, 0x00, 0x38], dtype=np.uint8)
+    A = torch.from_numpy(rng.choice(codes, size=(M, K)))
+    B = torch.from_numpy(rng.choice(codes, size=(N, K)))
+    sfa = torch.from_numpy(np.ldexp(1.0, rng.integers(-2, 3, size=(M, K // 128))).astype(np.float32))
+    sfb = torch.from_numpy(np.ldexp(1.0, rng.integers(-2, 3, size=(N // 128, K // 128))).astype(np.float32))
+    D = run_ue8m0(A, sfa, B, sfb, M, N)
+    assert dg.dg_device_status() == 0
+    np.testing.assert_array_equal(bf16_bits(D), O.gemm_fp8_nt(A, sfa, B, sfb))
+
+
+def test_ue8m0_reports_non_power_of_two_scales():
+    c = I.make_normal(I.seed_for(7, 1), 128, 256, 256)      # FP32 scales amax/448: not powers of two
+    run_ue8m0(c.A, c.sfa, c.B, c.sfb, 128, 256)
+    assert dg.dg_device_status() == 7                       # DG_SCALE_NOT_UE8M0
+    assert dg.dg_device_status() == 0                       # reported once, then cleared
