@@ -13,6 +13,7 @@ Workloads (--workload; one "step" = every case of the workload once, each on its
 * kgrouped: k-grouped FP32 weight gradient, G in {4, 8}, tokens per expert U[0.5, 1.5] x 4096 padded
   to 128, (M, N) in {(7168, 4096), (2048, 7168)}.
 * layouts: the M=4096 dense GEMMs with A and/or B stored transposed (TN, NN, TT).
+* ue8m0: the dense workload with power-of-two block scales on the block-scaled (UE8M0) path.
 
 Inputs are seeded synthetic N(0,1) values block-quantised to e4m3 (drawn on the GPU with the same
 counter-based generator the tests use on the CPU). Every case has its own buffers, so the working set of
@@ -57,6 +58,8 @@ WORKLOADS = {
                    "U[0.7,1.3] x {8192,4096} padded to 128, (N,K) in {(4096,7168),(7168,2048)}, BF16 out"),
     "masked": ("m-grouped masked FP8 GEMM (MoE decode), G in {1,2,4,16}, (max_m, expected_m) in {(256,64),"
                "(512,128),(1024,256)}, masked_m U[0.7,1.0] x expected_m, (N,K) in {(4096,7168),(7168,2048)}"),
+    "ue8m0": ("dense normal FP8 GEMM NT as the dense workload, with power-of-two block scales (amax/448 rounded up), "
+              "on the block-scaled UE8M0 tensor-core path, BF16 out"),
     "layouts": ("dense normal FP8 GEMM, M=4096, (N,K) as the dense workload, with transposed operand storage: "
                 "TN (A stored [K,M]), NN (B stored [K,N]), TT (both); BF16 out"),
     "kgrouped": ("k-grouped FP8 weight-gradient GEMM, FP32 accumulated, G in {4,8}, tokens per expert "
@@ -177,7 +180,16 @@ class Case:
         self.init_out = init_out          # output buffer contents that the call accumulates into
 
 
-def dense_cases(only=None):
+def ue8m0_cases():
+    """The dense workload's 18 GEMMs with power-of-two block scales, on the block-scaled (UE8M0) path."""
+    import moe_grouped_gemm_tma_gb300 as dg
+    cases = dense_cases(pow2=True)
+    for c in cases:
+        c.call = lambda d, o, s: dg.dg_gemm_fp8_nt_ue8m0(d["A"], d["sfa"], d["B"], d["sfb"], o, stream=s)
+    return cases
+
+
+def dense_cases(only=None, pow2=False):
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
     from oracle import oracle as O
@@ -185,7 +197,7 @@ def dense_cases(only=None):
     need = {}
     for (M, N, K) in shapes:
         need[(N, K)] = max(need.get((N, K), 0), M)
-    big = {(N, K): I.make_normal(I.seed_for(1, 0), M, N, K) for (N, K), M in need.items()}
+    big = {(N, K): I.make_normal(I.seed_for(1, 0), M, N, K, pow2=pow2) for (N, K), M in need.items()}
     cases = []
     for (M, N, K) in shapes:
         c = big[(N, K)]
@@ -301,7 +313,7 @@ def build_cases(workload, shape=None, only=None):
         cases = dense_cases(shape)
     else:
         cases = {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases,
-                 "layouts": layouts_cases}[workload]()
+                 "layouts": layouts_cases, "ue8m0": ue8m0_cases}[workload]()
     if only:
         cases = [c for c in cases if only in c.name]
         if not cases:

@@ -14,8 +14,10 @@
 //   warp 1      TMEM owner and MMA issuer: per K block four block-scaled MMAs (K = 32, scale bytes 0..3)
 //               into the tile's accumulator, then commits the stage and the scale slot; at the end of a
 //               tile commits the accumulator.
-//   warps 4..7  scale writers (one per TMEM lane quarter): per K block they turn the FP32 scales into
-//               exponents and store them with tcgen05.st into a TMEM scale slot: A's row m (lane m) in
+//   warp 2      scale stager: per K block, cp.async copies of the block's 128 sfa values and 4 sfb
+//               block rows into a shared-memory ring (as in dg_gemm_kernel), ahead of the writers.
+//   warps 4..7  scale writers (one per TMEM lane quarter): per K block they turn the staged FP32 scales
+//               into exponents and store them with tcgen05.st into a TMEM scale slot: A's row m (lane m) in
 //               four columns (the MMA reads row m's from column m / 32), B's row n (replicated in every
 //               lane quarter, lane n % 32) in column n / 32 after them. A scale that is not a power of two
 //               is reported (DG_SCALE_NOT_UE8M0).
@@ -39,7 +41,10 @@ struct CfgBS {
     static constexpr int OUT_WARPS = 4;
     static constexpr int STORE_BYTES = OUT_WARPS * 2048;
     static constexpr int STATIC_RESERVE = 640;
-    static constexpr int STAGES = ring_stages(STAGE_BYTES, 0, STORE_BYTES, STATIC_RESERVE);
+    static constexpr int SCALE_SLOTS = 16;                       // shared-memory ring of staged FP32 scales
+    static constexpr int SLOT_FLOATS = BM + 4;
+    static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
+    static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES, STORE_BYTES, STATIC_RESERVE);
     // TMEM: NACC accumulators of BN columns, then scale slots of 16 columns (A: 4, B: from +8, one per
     // 32 rows of B, at most 8)
     static constexpr int SLOT_COLS = 16;
@@ -48,7 +53,7 @@ struct CfgBS {
     static constexpr int SF_COL0 = NACC * BN;
     static constexpr int SLOTS_FIT = (TMEM_COLS - SF_COL0) / SLOT_COLS;
     static constexpr int SLOTS = SLOTS_FIT > 8 ? 8 : SLOTS_FIT;
-    static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + 1023) / 1024) * 1024;
+    static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + SCALE_BYTES + 1023) / 1024) * 1024;
     static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
     static_assert(SLOTS >= 2, "at least two scale slots");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
@@ -77,6 +82,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ uint64_t tmem_full_bar[NACC], tmem_empty_bar[NACC];
     __shared__ uint64_t sf_full_bar[SLOTS], sf_empty_bar[SLOTS];
+    __shared__ uint64_t scale_full_bar[C::SCALE_SLOTS], scale_empty_bar[C::SCALE_SLOTS];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
 
@@ -88,6 +94,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     uint8_t* smem = dyn_smem + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + STAGES * C::A_BYTES;
+    float* s_scales = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
     uint8_t* s_store = smem + C::STORE_OFF;
 
     if (threadIdx.x == 0) {
@@ -102,6 +109,10 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         for (int s = 0; s < SLOTS; ++s) {
             mbar_init(&sf_full_bar[s], 4);
             mbar_init(&sf_empty_bar[s], 1);
+        }
+        for (int s = 0; s < C::SCALE_SLOTS; ++s) {
+            mbar_init(&scale_full_bar[s], 32);
+            mbar_init(&scale_empty_bar[s], 4);
         }
         s_abort = 0;
         fence_mbar_init();
@@ -212,36 +223,69 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             if (++acc == NACC) { acc = 0; aphase ^= 1u; }
         }
         if (!ok && any && issuer) drain_wait(&tmem_full_bar[last_acc], last_parity);
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------------- scale stager
+        int slot = 0;
+        uint32_t sphase = 0;
+        for (int t = unit; t < num_tiles; t += num_units) {
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const float* sfa_rows[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sfa_rows[i] = p.sfa + static_cast<size_t>(min(ti.a_row + lane + 32 * i, p.rows - 1)) * p.kbs + ti.kb0;
+            const float* sfb_src = p.sfb + static_cast<size_t>(min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1)) * p.kbs + ti.kb0;
+            bool ok = true;
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                float* dst = s_scales + slot * C::SLOT_FLOATS;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + kb);
+                if (lane < 4) cp_async_4(dst + BM + lane, sfb_src + kb);
+                cp_async_arrive_noinc(&scale_full_bar[slot]);
+                if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+            }
+            if (!ok) break;
+        }
+        cp_async_wait_all();
     } else if (warp >= 4 && warp < 8) {
         // ---------------------------------------------------------------------- scale writers
         const int q = warp & 3;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        int slot = 0;
-        uint32_t sphase = 0;
+        int slot = 0, sslot = 0;
+        uint32_t tphase = 0, sphase = 0;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
             const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
-            const float* sfa_row = p.sfa + static_cast<size_t>(min(ti.m0 + q * 32 + lane, p.rows - 1)) * p.kbs + ti.kb0;
-            // B scale rows of this lane's columns n0 + 32 j + lane (j < 8; columns past N reuse the last)
-            const float* sfb_rows[8];
+            // staged sfb block row of this lane's columns n0 + 32 j + lane (columns past N reuse the last)
+            int bidx[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                sfb_rows[j] = p.sfb + static_cast<size_t>(min(ti.n0 + 32 * j + lane, p.n - 1) / 128) * p.kbs + ti.kb0;
+            for (int j = 0; j < 8; ++j) bidx[j] = min(min(ti.n0 + 32 * j + lane, p.n - 1) / 128 - ti.n0 / 128, 3);
             for (int kb = 0; kb < ti.nkb; ++kb) {
-                const bool got = wait_bounded(&sf_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                bool got = (static_cast<unsigned>(mbar_try_wait(&sf_empty_bar[slot], tphase ^ 1u)) &
+                            static_cast<unsigned>(mbar_try_wait(&scale_full_bar[sslot], sphase))) != 0u;
+                if (!got)
+                    got = wait_bounded(&sf_empty_bar[slot], tphase ^ 1u, abort_flag, p.status) &&
+                          wait_bounded(&scale_full_bar[sslot], sphase, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                const uint32_t va = ue8m0x4(sfa_row[kb], p.status);
+                const float* sl = s_scales + sslot * C::SLOT_FLOATS;
+                const uint32_t va = ue8m0x4(sl[q * 32 + lane], p.status);
+                const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
                 uint32_t vb[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(sfb_rows[j][kb], p.status) : 0u;
+                for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), p.status) : 0u;
                 const uint32_t col = static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
                 tmem_st_x4(lane_base + col, va, va, va, va);
                 tmem_st_x8(lane_base + col + C::SFB_OFF, vb);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sf_full_bar[slot]);
-                if (++slot == SLOTS) { slot = 0; sphase ^= 1u; }
+                if (lane == 0) {
+                    mbar_arrive(&sf_full_bar[slot]);
+                    mbar_arrive(&scale_empty_bar[sslot]);
+                }
+                if (++slot == SLOTS) { slot = 0; tphase ^= 1u; }
+                if (++sslot == C::SCALE_SLOTS) { sslot = 0; sphase ^= 1u; }
             }
         }
     } else if (warp >= 8) {
