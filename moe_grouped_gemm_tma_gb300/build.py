@@ -14,7 +14,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdg.so")
 
 SOURCES = ["dg_api.cu", "dg_inst_normal.cu", "dg_inst_contiguous.cu", "dg_inst_masked.cu", "dg_inst_kgrouped.cu",
-           "dg_inst_bs.cu"]
+           "dg_inst_bs.cu", "dg_inst_swap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

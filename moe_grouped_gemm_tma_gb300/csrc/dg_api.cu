@@ -380,6 +380,56 @@ static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B,
     const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
+    const int kbs = K / 128;
+    if (!a_mn && !b_mn && !pair && M <= 128) {
+        // Few rows: the swapped-operand kernel stages 128 B rows plus M A rows per K block instead of
+        // 128 A rows plus BN B rows. Take it when it moves fewer operand bytes per CTA (waves x K blocks
+        // per CTA x bytes per K block) and each CTA streams a long K (its per-tile exchange, column
+        // stores and reduction cost more than they save below ~32 K blocks: measured 64 x 7168 x 16384
+        // 47.7 -> 37.5 us, while 128 x 7168 x 2048 went 15 -> 19 us); DG_SWAP=0 / 1 forces the choice.
+        const int bmt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
+        const int nt = cdiv(N, 128);
+        int s_sw = 1;
+        for (int s = 2; s <= 4; s *= 2)
+            if (kbs >= 4 * s && static_cast<int64_t>(nt) * s <= dev.sms) s_sw = s;
+        const int64_t cost_sw = cdiv(static_cast<int64_t>(nt) * s_sw, dev.sms) * cdiv(kbs, s_sw) *
+                                static_cast<int64_t>(bmt * 128 + 128 * 128);
+        const int64_t tiles_std = static_cast<int64_t>(cdiv(M, BM)) * cdiv(N, bn);
+        const int64_t cost_std = cdiv(tiles_std * split, dev.sms) * cdiv(kbs, split) *
+                                 static_cast<int64_t>(128 * 128 + bn * 128);
+        bool swap = cost_sw < cost_std && cdiv(kbs, s_sw) >= 32;
+        if (const char* e = getenv("DG_SWAP")) swap = (e[0] == '1');
+        if (swap) {
+            if (make_operand_map(&L.tmap_a, A, M, K, bmt) != DG_OK) return DG_CUDA_ERROR;
+            if (make_operand_map(&L.tmap_b, B, N, K, 128) != DG_OK) return DG_CUDA_ERROR;
+            if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
+            Params& p = L.params;
+            p.sfa = sfa;
+            p.sfb = sfb;
+            p.d = D;
+            p.status = dev.status;
+            p.rows = M;
+            p.n = N;
+            p.kbs = kbs;
+            p.groups = 1;
+            p.sfb_rows = cdiv(N, 128);
+            p.m_blocks = cdiv(M, bmt);
+            p.n_blocks = nt;
+            p.group_m = 1;
+            p.split = s_sw;
+            p.tiles = p.m_blocks * p.n_blocks;
+            L.units = p.tiles;
+            L.sms = dev.sms;
+            L.stream = stream;
+            cudaError_t e = cudaErrorInvalidValue;
+            switch (bmt) {
+                case 32: e = launch_swap<32>(L); break;
+                case 64: e = launch_swap<64>(L); break;
+                case 128: e = launch_swap<128>(L); break;
+            }
+            return e == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+        }
+    }
     if ((a_mn ? make_mn_operand_map(&L.tmap_a, A, K, M) : make_operand_map(&L.tmap_a, A, M, K, BM)) != DG_OK)
         return DG_CUDA_ERROR;
     if ((b_mn ? make_mn_operand_map(&L.tmap_b, B, K, N) : make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair)) != DG_OK)

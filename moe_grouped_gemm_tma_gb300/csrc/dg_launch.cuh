@@ -28,6 +28,10 @@ cudaError_t launch(const Launch& L);
 template <int BN>
 cudaError_t launch_bs(const Launch& L);
 
+// The swapped-operand normal GEMM for few rows (dg_inst_swap.cu).
+template <int BMT>
+cudaError_t launch_swap(const Launch& L);
+
 // Programmatic dependent launch is on unless DG_PDL=0.
 inline bool pdl_enabled() {
     static const bool on = [] {

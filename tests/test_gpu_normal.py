@@ -114,3 +114,30 @@ def test_dense_workload_sampled_rows(N, K):
         rows = sample_rows(M, 24, seed=M + N + K)
         want = O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb, rows=rows)
         check_bf16(bf16_bits(D)[rows], want, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 256, 128), (17, 1000, 512), (33, 200, 384), (50, 4096, 2048), (64, 7168, 2048), (100, 2112, 1024),
+    (128, 4096, 7168), (64, 2112, 7168),
+])
+def test_swapped_small_m(M, N, K, monkeypatch):
+    # the swapped-operand kernel for few rows (D^T = B . A^T on the tensor cores), with its split-K
+    # clusters, on ragged M and N
+    monkeypatch.setenv("DG_SWAP", "1")
+    c = I.make_normal(I.seed_for(1, 500 + M + N + K), M, N, K)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"swapped {M}x{N}x{K}")
+
+
+def test_swapped_integer_exact_bitwise(monkeypatch):
+    monkeypatch.setenv("DG_SWAP", "1")
+    rng = np.random.default_rng(21)
+    M, N, K = 96, 512, 512
+    codes = np.array([0xB8, 0x00, 0x38], dtype=np.uint8)
+    A = torch.from_numpy(rng.choice(codes, size=(M, K)))
+    B = torch.from_numpy(rng.choice(codes, size=(N, K)))
+    sfa, sfb = torch.ones(M, K // 128), torch.ones(N // 128, K // 128)
+    D = sentinel_bf16(M, N)
+    dg.dg_gemm_fp8_nt(dev(A), dev(sfa), dev(B), dev(sfb), D)
+    assert dg.dg_device_status() == 0
+    np.testing.assert_array_equal(bf16_bits(D), O.gemm_fp8_nt(A, sfa, B, sfb))
