@@ -118,24 +118,34 @@ struct Cfg {
     static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
     // output staging for TMA stores: per epilogue warp STORE_SLOTS 1 KB boxes of 32 rows x 32 bytes (16 BF16
     // columns, or 8 FP32 columns added into the k-grouped output)
+    // Epilogue warpgroups (each a column block of the tile); the launch's registers are re-split so
+    // that the control warpgroup keeps CTRL_REGS. Three (512 threads, 152 registers each, 64 columns
+    // per thread) measured slower than two for the k-grouped layout at BN = 192 (1353 against 1570
+    // TFLOP/s), so every specialisation uses two.
+    static constexpr int NWG = 2;
+    static constexpr int EPI_WARPS_C = 4 * NWG;
+    static constexpr int THREADS_C = 128 + 32 * EPI_WARPS_C;
+    static constexpr int LAUNCH_REGS = ((65536 / THREADS_C) / 8) * 8;
+    static constexpr int EPI_REGS_C = ((THREADS_C * LAUNCH_REGS - 128 * CTRL_REGS) / (THREADS_C - 128) / 8) * 8;
     static constexpr int STORE_SLOTS = 2;                        // 1 KB boxes in flight per epilogue warp
-    static constexpr int STORE_BYTES = EPI_WARPS * STORE_SLOTS * 1024;
+    static constexpr int STORE_BYTES = EPI_WARPS_C * STORE_SLOTS * 1024;
     // static shared memory: barriers and flags (under 640 bytes), plus the masked prefix table
     static constexpr int STATIC_RESERVE = 640 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
     // Narrow tiles: the two epilogue warpgroups take alternate K blocks over all BN columns (two
     // independent per-block chains in flight) instead of one column half each; once per tile each hands
     // the other the half it does not store, XCHG_PASS columns at a time through shared memory.
-    static constexpr bool KPAR = (BN <= 64 && MODE != kKGrouped);
+    static constexpr bool KPAR = (BN <= 64 && MODE != kKGrouped && NWG == 2);
     static constexpr int XCHG_PASS = (BN / 2) < 32 ? (BN / 2) : 32;
     static constexpr int XCHG_BYTES = KPAR ? 2 * BM * XCHG_PASS * 4 : 0;
-    static constexpr int EPI_ARRIVALS = KPAR ? EPI_WARPS / 2 : EPI_WARPS;   // warps releasing one block
+    static constexpr int EPI_ARRIVALS = KPAR ? EPI_WARPS_C / 2 : EPI_WARPS_C;   // warps releasing one block
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
     static constexpr int NACC = NACC_FIT > 8 ? 8 : NACC_FIT;
     static constexpr int XCHG_OFF = STAGES * STAGE_BYTES + SCALE_BYTES;
     static constexpr int STORE_OFF = ((XCHG_OFF + XCHG_BYTES + 1023) / 1024) * 1024;
     static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
-    static constexpr int COLS = BN / 2;        // columns per epilogue warpgroup
+    static constexpr int COLS = BN / NWG;      // columns per epilogue warpgroup
+    static_assert(COLS % 16 == 0, "each epilogue warpgroup takes whole 16-column chunks");
     static constexpr int CHUNKS = COLS / 16;   // 16-column TMEM loads per K block
     // Epilogue TMEM loads per K block come in batches of EPI_GC chunks, each batch waited on once.
     // Double-buffered (EPI_DB): batch g+1 is in flight while batch g is promoted. Single-buffered:
@@ -303,7 +313,7 @@ __device__ __forceinline__ void promote_chunk(float (&accum)[COLS], const uint32
 }
 
 template <int MODE, int BN, int PAIR>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<MODE, BN, PAIR>::THREADS_C, 1)
 dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ Params p) {
     using C = Cfg<MODE, BN, PAIR>;
@@ -358,8 +368,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             mbar_init(&scale_empty_bar[s], C::EPI_ARRIVALS);
         }
         {
-            mbar_init(&xchg_full_bar, EPI_WARPS);
-            mbar_init(&xchg_free_bar, EPI_WARPS);
+            mbar_init(&xchg_full_bar, C::EPI_WARPS_C);
+            mbar_init(&xchg_free_bar, C::EPI_WARPS_C);
         }
         s_abort = 0;
         fence_mbar_init();
@@ -380,7 +390,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     grid_launch_dependents();
     if (MODE == kMasked) {
         // per-expert tile counts, then an exclusive prefix sum (one warp)
-        for (int g = threadIdx.x; g < p.groups; g += THREADS) {
+        for (int g = threadIdx.x; g < p.groups; g += C::THREADS_C) {
             const int mm = min(max(__ldg(p.masked_m + g), 0), p.rows);
             s_prefix[g + 1] = ((mm + C::TILE_M - 1) / C::TILE_M) * p.n_blocks;
         }
@@ -611,10 +621,10 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ promotion + epilogue
-        regs_inc<EPI_REGS>();
+        regs_inc<C::EPI_REGS_C>();
         const int ew = warp - EPI_WARP0;       // 0..7
         const int q = warp & 3;                // TMEM lane quarter this warp may access
-        const int h = ew >> 2;                 // column half of the tile
+        const int h = ew >> 2;                 // epilogue warpgroup: its column block of the tile
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * COLS;
         uint32_t xphase = 0;                   // narrow-tile exchange rounds so far (parity)
@@ -892,7 +902,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             const int rows_per = BM / p.split;
             const int groups = rows_per * (BN / 4);
             const uint32_t part_local = smem_u32(smem);
-            for (int gi = static_cast<int>(threadIdx.x) - EPI_WARP0 * 32; gi < groups; gi += EPI_WARPS * 32) {
+            for (int gi = static_cast<int>(threadIdx.x) - EPI_WARP0 * 32; gi < groups; gi += C::EPI_WARPS_C * 32) {
                 const int row = srank * rows_per + gi / (BN / 4);
                 const int c4 = (gi % (BN / 4)) * 4;
                 const uint32_t off = static_cast<uint32_t>((row * C::PSTRIDE + c4) * 4);

@@ -65,7 +65,8 @@ cudaError_t launch(const Launch& L) {
             cudaFuncAttributes fa;
             e = cudaFuncGetAttributes(&fa, kern);
             if (e != cudaSuccess) return e;
-            if (fa.numRegs * THREADS != CTRL_REGS * 128 + EPI_REGS * (THREADS - 128)) return cudaErrorInvalidConfiguration;
+            if (fa.numRegs * C::THREADS_C != CTRL_REGS * 128 + C::EPI_REGS_C * (C::THREADS_C - 128))
+                return cudaErrorInvalidConfiguration;
             if (PAIR == 2) {
                 cudaLaunchConfig_t q = {};
                 cudaLaunchAttribute qa[1];
@@ -75,7 +76,7 @@ cudaError_t launch(const Launch& L) {
                 qa[0].val.clusterDim.z = 1;
                 q.attrs = qa;
                 q.numAttrs = 1;
-                q.blockDim = dim3(THREADS, 1, 1);
+                q.blockDim = dim3(C::THREADS_C, 1, 1);
                 q.dynamicSmemBytes = C::DYN_SMEM;
                 q.gridDim = dim3(2u * static_cast<unsigned>(L.sms / 2), 1, 1);
                 int clusters = 0;
@@ -88,7 +89,7 @@ cudaError_t launch(const Launch& L) {
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(C::THREADS_C, 1, 1);
     cfg.dynamicSmemBytes = C::DYN_SMEM;
     cfg.stream = L.stream;
     if (MODE == kNormal && PAIR == 1 && L.params.split > 1) {
