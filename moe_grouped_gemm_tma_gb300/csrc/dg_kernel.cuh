@@ -113,7 +113,9 @@ struct Cfg {
     // scale slot: sfa of the CTA's 128 rows, then sfb: 4 block rows (from n0/128), or BN per-row values
     static constexpr int SB = (MODE == kKGrouped) ? BN : 4;
     static constexpr int SLOT_FLOATS = BM + SB;
-    // the k-grouped slots hold BN per-column values, so they get a shallower ring
+    // the k-grouped slots hold BN per-column values, so they get a shallower ring (eight: six would
+    // leave room for a fifth operand stage at BN = 192, but the stager's scattered per-column loads
+    // then fall behind, measured 15% slower)
     static constexpr int SCALE_SLOTS = (MODE == kKGrouped) ? 8 : SCALE_SLOTS_MAX;
     static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
     // output staging for TMA stores: per epilogue warp STORE_SLOTS 1 KB boxes of 32 rows x 32 bytes (16 BF16
