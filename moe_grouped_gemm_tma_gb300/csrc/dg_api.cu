@@ -113,6 +113,19 @@ dg_status make_output_map(CUtensorMap* m, void* base, int64_t rows, int64_t n) {
     return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
 }
 
+// Row-major BF16 output [rows, n] written in boxes of 32 rows x 32 columns (64 bytes) with the
+// 64-byte swizzle of the main kernel's whole-tile staging.
+dg_status make_tile_output_map(CUtensorMap* m, void* base, int64_t rows, int64_t n) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(n) * 2};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
+}
+
 // FP32 weight gradient [G][M][N] (N contiguous) added into in boxes of 1 x 32 rows x 8 columns (32
 // bytes) with the 32-byte swizzle; the third dimension keeps each box inside its expert's M rows.
 dg_status make_wgrad_map(CUtensorMap* m, float* base, int64_t g, int64_t rows, int64_t n) {
@@ -434,7 +447,7 @@ static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B,
         return DG_CUDA_ERROR;
     if ((b_mn ? make_mn_operand_map(&L.tmap_b, B, K, N) : make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair)) != DG_OK)
         return DG_CUDA_ERROR;
-    if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
+    if (make_tile_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
     p.sfb = sfb;
@@ -574,7 +587,7 @@ dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, Mt, K, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_output_map(&L.tmap_d, D, Mt, N) != DG_OK) return DG_CUDA_ERROR;
+    if (make_tile_output_map(&L.tmap_d, D, Mt, N) != DG_OK) return DG_CUDA_ERROR;
     if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
@@ -624,7 +637,7 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, static_cast<int64_t>(G) * max_m, K, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_output_map(&L.tmap_d, D, static_cast<int64_t>(G) * max_m, N) != DG_OK) return DG_CUDA_ERROR;
+    if (make_tile_output_map(&L.tmap_d, D, static_cast<int64_t>(G) * max_m, N) != DG_OK) return DG_CUDA_ERROR;
     if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;

@@ -118,8 +118,6 @@ struct Cfg {
     // then fall behind, measured 15% slower)
     static constexpr int SCALE_SLOTS = (MODE == kKGrouped) ? 8 : SCALE_SLOTS_MAX;
     static constexpr int SCALE_BYTES = SCALE_SLOTS * SLOT_FLOATS * 4;
-    // output staging for TMA stores: per epilogue warp STORE_SLOTS 1 KB boxes of 32 rows x 32 bytes (16 BF16
-    // columns, or 8 FP32 columns added into the k-grouped output)
     // Epilogue warpgroups (each a column block of the tile); the launch's registers are re-split so
     // that the control warpgroup keeps CTRL_REGS. Three (512 threads, 152 registers each, 64 columns
     // per thread) measured slower than two for the k-grouped layout at BN = 192 (1353 against 1570
@@ -129,8 +127,7 @@ struct Cfg {
     static constexpr int THREADS_C = 128 + 32 * EPI_WARPS_C;
     static constexpr int LAUNCH_REGS = ((65536 / THREADS_C) / 8) * 8;
     static constexpr int EPI_REGS_C = ((THREADS_C * LAUNCH_REGS - 128 * CTRL_REGS) / (THREADS_C - 128) / 8) * 8;
-    static constexpr int STORE_SLOTS = 2;                        // 1 KB boxes in flight per epilogue warp
-    static constexpr int STORE_BYTES = EPI_WARPS_C * STORE_SLOTS * 1024;
+    static constexpr int COLS = BN / NWG;      // columns per epilogue warpgroup
     // static shared memory: barriers and flags (under 640 bytes), plus the masked prefix table
     static constexpr int STATIC_RESERVE = 640 + (MODE == kMasked ? 4 * (MAX_MASKED_G + 1) : 0);
     // Narrow tiles: the two epilogue warpgroups take alternate K blocks over all BN columns (two
@@ -140,13 +137,23 @@ struct Cfg {
     static constexpr int XCHG_PASS = (BN / 2) < 32 ? (BN / 2) : 32;
     static constexpr int XCHG_BYTES = KPAR ? 2 * BM * XCHG_PASS * 4 : 0;
     static constexpr int EPI_ARRIVALS = KPAR ? EPI_WARPS_C / 2 : EPI_WARPS_C;   // warps releasing one block
+    // Output staging. BF16 out, where it fits next to a ring of at least four stages: the whole CTA tile
+    // (each epilogue warp its 32 rows x COLS columns as boxes of 32 x 32 with the 64-byte swizzle),
+    // written by TMA stores that the warp does not wait for until it stages its next tile (a tile's
+    // 64 KB take the SM's store path several thousand cycles, which would otherwise stall promotion).
+    // Otherwise 2 KB per epilogue warp: for the k-grouped FP32 output STORE_SLOTS TMA boxes of 32 rows x
+    // 8 columns in flight; for BF16 out one buffer of 32 rows x 32 columns, written with plain stores.
+    static constexpr int STORE_SLOTS = 2;
+    static constexpr bool FULL_STAGE = MODE != kKGrouped && COLS % 32 == 0 &&
+        ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, BM * BN * 2, STATIC_RESERVE) >= 4;
+    static constexpr int STORE_WARP_BYTES = FULL_STAGE ? 32 * COLS * 2 : STORE_SLOTS * 1024;
+    static constexpr int STORE_BYTES = EPI_WARPS_C * STORE_WARP_BYTES;
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
     static constexpr int NACC = NACC_FIT > 8 ? 8 : NACC_FIT;
     static constexpr int XCHG_OFF = STAGES * STAGE_BYTES + SCALE_BYTES;
     static constexpr int STORE_OFF = ((XCHG_OFF + XCHG_BYTES + 1023) / 1024) * 1024;
     static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
-    static constexpr int COLS = BN / NWG;      // columns per epilogue warpgroup
     static_assert(COLS % 16 == 0, "each epilogue warpgroup takes whole 16-column chunks");
     static constexpr int CHUNKS = COLS / 16;   // 16-column TMEM loads per K block
     // Epilogue TMEM loads per K block come in batches of EPI_GC chunks, each batch waited on once.
@@ -850,41 +857,105 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         bulk_commit();
                     }
                 }
-            } else if (MODE != kMasked || ti.rows_valid >= BM) {
-                // Stage 32 rows x 16 columns per round in one of the warp's 1 KB slots (32-byte
-                // swizzle: a row's two 16-byte chunks swap places every 4 rows, so the warp's stores
-                // hit all banks), then one lane issues the TMA store of the box; TMA clips rows and
-                // columns outside D. A half is rewritten only after its previous box has been read.
-                uint8_t* wbuf = s_store + ew * (C::STORE_SLOTS * 1024);
-                const int y = ti.d_row + q * 32;
-                const int sw = (lane >> 2) & 1;
+            } else if constexpr (C::FULL_STAGE) {
+                // BF16 out: the warp's 32 rows x COLS columns go to its staging boxes (32 x 32, 64 bytes a
+                // row, 16-byte chunks swizzled by row pair as the 64-byte TMA swizzle expects: chunk ^
+                // ((row >> 1) & 3); eight consecutive lanes touch every bank once), then one lane issues
+                // the TMA stores and the warp moves on. The boxes are rewritten one tile later, after
+                // their previous stores have read them. A masked tile with rows past masked_m is written
+                // with plain stores of its valid rows instead (four lanes a row, 16 bytes each).
+                uint8_t* wbuf = s_store + ew * C::STORE_WARP_BYTES;
+                if (lane == 0) bulk_wait_read_n<0>();
+                __syncwarp();
 #pragma unroll
-                for (int c = 0; c < CHUNKS; ++c) {
-                    uint8_t* half = wbuf + (store_round % C::STORE_SLOTS) * 1024;
-                    ++store_round;
-                    if (lane == 0) bulk_wait_read_n<C::STORE_SLOTS - 1>();
-                    __syncwarp();
-                    uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
-                    rowp[sw] = make_uint4(pack_bf16x2(accum[c * 16 + 0], accum[c * 16 + 1]), pack_bf16x2(accum[c * 16 + 2], accum[c * 16 + 3]),
-                                          pack_bf16x2(accum[c * 16 + 4], accum[c * 16 + 5]), pack_bf16x2(accum[c * 16 + 6], accum[c * 16 + 7]));
-                    rowp[sw ^ 1] = make_uint4(pack_bf16x2(accum[c * 16 + 8], accum[c * 16 + 9]), pack_bf16x2(accum[c * 16 + 10], accum[c * 16 + 11]),
-                                              pack_bf16x2(accum[c * 16 + 12], accum[c * 16 + 13]), pack_bf16x2(accum[c * 16 + 14], accum[c * 16 + 15]));
+                for (int r = 0; r < COLS / 32; ++r) {
+                    uint4* mine = reinterpret_cast<uint4*>(wbuf + r * 2048 + lane * 64);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int j = r * 32 + c * 8;
+                        mine[c ^ ((lane >> 1) & 3)] = make_uint4(pack_bf16x2(accum[j], accum[j + 1]), pack_bf16x2(accum[j + 2], accum[j + 3]),
+                                                                 pack_bf16x2(accum[j + 4], accum[j + 5]), pack_bf16x2(accum[j + 6], accum[j + 7]));
+                    }
+                }
+                if (MODE != kMasked || ti.rows_valid >= BM) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmap_d, half, cstart + c * 16, y);
+#pragma unroll
+                        for (int r = 0; r < COLS / 32; ++r) tma_store_2d(&tmap_d, wbuf + r * 2048, cstart + r * 32, ti.d_row + q * 32);
                         bulk_commit();
                     }
-                }
-            } else if (row_in_tile < ti.rows_valid) {
-                // a masked tile with rows past masked_m: plain stores of the valid rows only
-                __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.d) +
-                                      static_cast<size_t>(ti.d_row + row_in_tile) * p.n + cstart;
+                } else {
+                    __syncwarp();
+                    __nv_bfloat16* dtile = reinterpret_cast<__nv_bfloat16*>(p.d) + static_cast<size_t>(ti.d_row + q * 32) * p.n;
+                    const int rows_here = ti.rows_valid - q * 32;
+                    const int cc = lane & 3;
 #pragma unroll
-                for (int j = 0; j < COLS; j += 8)
-                    if (cstart + j < p.n)
-                        st_global_v4(drow + j, pack_bf16x2(accum[j], accum[j + 1]), pack_bf16x2(accum[j + 2], accum[j + 3]),
-                                     pack_bf16x2(accum[j + 4], accum[j + 5]), pack_bf16x2(accum[j + 6], accum[j + 7]));
+                    for (int r = 0; r < COLS / 32; ++r) {
+                        const int col = cstart + r * 32 + cc * 8;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = i * 8 + (lane >> 2);
+                            const uint4 v = *reinterpret_cast<const uint4*>(wbuf + r * 2048 + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4));
+                            if (row < rows_here && col < p.n)
+                                st_global_v4(dtile + static_cast<size_t>(row) * p.n + col, v.x, v.y, v.z, v.w);
+                        }
+                    }
+                }
+            } else {
+                // BF16 out through the warp's 2 KB staging buffer, 32 columns a round: each lane writes
+                // its row's 64 bytes, then four lanes a row read them back and store 16 bytes each, so
+                // one store instruction covers eight rows of 64 contiguous bytes (whole sectors). The
+                // 16-byte chunks of a row are swizzled by row pair (chunk ^ ((row >> 1) & 3)): eight
+                // consecutive lanes touch every bank once, writing and reading. A 16-column tail round
+                // uses two lanes a row (chunk ^ ((row >> 2) & 1)). Rows past rows_valid (the matrix
+                // edge, or masked_m) and columns past N are not written. Plain stores need no proxy
+                // fence or bulk-store wait, and are not waited on: the warp moves on to its next tile.
+                uint8_t* wbuf = s_store + ew * C::STORE_WARP_BYTES;
+                __nv_bfloat16* dtile = reinterpret_cast<__nv_bfloat16*>(p.d) + static_cast<size_t>(ti.d_row + q * 32) * p.n;
+                const int rows_here = ti.rows_valid - q * 32;   // valid rows of this warp's 32
+#pragma unroll
+                for (int r = 0; r < COLS / 32; ++r) {
+                    __syncwarp();   // the previous round's reads are done
+                    uint4* mine = reinterpret_cast<uint4*>(wbuf + lane * 64);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int j = r * 32 + c * 8;
+                        mine[c ^ ((lane >> 1) & 3)] = make_uint4(pack_bf16x2(accum[j], accum[j + 1]), pack_bf16x2(accum[j + 2], accum[j + 3]),
+                                                                 pack_bf16x2(accum[j + 4], accum[j + 5]), pack_bf16x2(accum[j + 6], accum[j + 7]));
+                    }
+                    __syncwarp();
+                    const int cc = lane & 3;
+                    const int col = cstart + r * 32 + cc * 8;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = i * 8 + (lane >> 2);
+                        const uint4 v = *reinterpret_cast<const uint4*>(wbuf + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4));
+                        if (row < rows_here && col < p.n)
+                            st_global_v4(dtile + static_cast<size_t>(row) * p.n + col, v.x, v.y, v.z, v.w);
+                    }
+                }
+                if constexpr (COLS % 32 != 0) {
+                    constexpr int j0 = (COLS / 32) * 32;
+                    __syncwarp();
+                    uint4* mine = reinterpret_cast<uint4*>(wbuf + lane * 32);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int j = j0 + c * 8;
+                        mine[c ^ ((lane >> 2) & 1)] = make_uint4(pack_bf16x2(accum[j], accum[j + 1]), pack_bf16x2(accum[j + 2], accum[j + 3]),
+                                                                 pack_bf16x2(accum[j + 4], accum[j + 5]), pack_bf16x2(accum[j + 6], accum[j + 7]));
+                    }
+                    __syncwarp();
+                    const int cc = lane & 1;
+                    const int col = cstart + j0 + cc * 8;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int row = i * 16 + (lane >> 1);
+                        const uint4 v = *reinterpret_cast<const uint4*>(wbuf + row * 32 + ((cc ^ ((row >> 2) & 1)) << 4));
+                        if (row < rows_here && col < p.n)
+                            st_global_v4(dtile + static_cast<size_t>(row) * p.n + col, v.x, v.y, v.z, v.w);
+                    }
+                }
             }
         }
         // every TMA store of this warp has completed (and released its staging buffer) before exit
