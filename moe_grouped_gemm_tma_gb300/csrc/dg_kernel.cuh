@@ -164,8 +164,12 @@ struct Cfg {
     // already: a pass costs several hundred cycles of barrier round trips, more than the MMA of a narrow
     // block. (Measured: it slows the wide two-accumulator tiles of the other layouts.)
     static constexpr bool KB_PAIRING = (NACC >= 4) || MODE == kKGrouped;
-    static constexpr int EPI_GC = (MODE == kKGrouped && COLS > 96) ? 1 : 2;
-    static constexpr bool EPI_DB = true;
+    // Up to 96 columns a thread, a whole K block fits in registers beside the running sums: all its loads
+    // are issued and waited on once, and the accumulator is released before any FMA, which keeps the
+    // promotion arithmetic off the two-accumulator MMA -> release -> MMA loop.
+    static constexpr bool EPI_ONE = MODE != kKGrouped && COLS <= 96;
+    static constexpr int EPI_GC = EPI_ONE ? CHUNKS : ((MODE == kKGrouped && COLS > 96) ? 1 : 2);
+    static constexpr bool EPI_DB = !EPI_ONE;
     // split-K partial sums: [128 rows][BN + 4] FP32 (padded rows: conflict-free 16-byte stores), in the
     // operand ring, which is idle once the tile's last MMA has completed
     static constexpr int PSTRIDE = BN + 4;
