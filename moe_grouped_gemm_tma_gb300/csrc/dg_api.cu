@@ -631,8 +631,21 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
 
     const int hint = (expected_m > 0 && expected_m < max_m) ? expected_m : max_m;
     const bool pair = use_pair(hint);
-    const Spec sp = pair ? spec_override(kMaskedSpecs2, choose_spec(kMaskedSpecs2, static_cast<int64_t>(G) * cdiv(hint, 2 * BM), N, dev.sms))
-                         : spec_override(kMaskedSpecs1, choose_spec(kMaskedSpecs1, static_cast<int64_t>(G) * cdiv(hint, BM), N, dev.sms));
+    Spec sp = pair ? spec_override(kMaskedSpecs2, choose_spec(kMaskedSpecs2, static_cast<int64_t>(G) * cdiv(hint, 2 * BM), N, dev.sms))
+                   : spec_override(kMaskedSpecs1, choose_spec(kMaskedSpecs1, static_cast<int64_t>(G) * cdiv(hint, BM), N, dev.sms));
+    int split = 1;
+    if (!pair) {
+        // Split-K when the expected tiles (from expected_m) fill under half the SMs. The launch holds a
+        // cluster for every possible tile (the count is known only on the device), and clusters past the
+        // count still pay their set-up, so the split is dropped when that grid exceeds two waves
+        // (measured with one expert of 59 rows, N = 4096, K = 7168: 25.2 -> 23.2 us at max_m = 256; at
+        // max_m = 512, four waves of mostly empty clusters, 24.6 -> 26.9 us).
+        Spec s2 = sp;
+        split = choose_split(kMaskedSpecs1, &s2, static_cast<int64_t>(G) * cdiv(hint, BM), N, K / 128, dev.sms);
+        if (split > 1 && static_cast<int64_t>(G) * cdiv(max_m, BM) * cdiv(N, s2.bn) * split > 2 * static_cast<int64_t>(dev.sms))
+            split = 1;
+        if (split > 1) sp = s2;
+    }
     const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
@@ -655,6 +668,7 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     const int64_t max_tiles = static_cast<int64_t>(G) * p.m_blocks * p.n_blocks;
     if (max_tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = 0;  // counted on the device from masked_m
+    p.split = split;
     L.units = static_cast<int>(max_tiles);
     L.sms = dev.sms;
     L.stream = stream;

@@ -174,7 +174,7 @@ struct Cfg {
     // operand ring, which is idle once the tile's last MMA has completed
     static constexpr int PSTRIDE = BN + 4;
     static constexpr int PARTIAL_BYTES = BM * PSTRIDE * 4;
-    static_assert(!(MODE == kNormal && PAIR == 1) || PARTIAL_BYTES <= STAGES * STAGE_BYTES,
+    static_assert(!((MODE == kNormal || MODE == kMasked) && PAIR == 1) || PARTIAL_BYTES <= STAGES * STAGE_BYTES,
                   "split-K partials must fit in the operand ring");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte swizzle-atom alignment");
@@ -240,6 +240,10 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
         ti.d_row = ti.a_row;
         ti.b_row = g * p.n + ti.n0 + rank * B_ROWS;
         ti.rows_valid = min(BM, mm - ti.m0);
+        if (p.split > 1) {   // this CTA's share of the tile's K blocks
+            ti.kb0 = (srank * p.kbs) / p.split;
+            ti.nkb = ((srank + 1) * p.kbs) / p.split - ti.kb0;
+        }
     } else {  // kKGrouped
         const int per_g = p.m_blocks * p.n_blocks;
         const int g = t / per_g, local = t - g * per_g;
@@ -348,7 +352,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // split-K: a cluster of p.split CTAs shares one tile (one tile per cluster), each CTA a K range
-    const bool split_k = (MODE == kNormal && PAIR == 1 && p.split > 1);
+    const bool split_k = ((MODE == kNormal || MODE == kMasked) && PAIR == 1 && p.split > 1);
     const int crank = (PAIR == 2 || split_k) ? static_cast<int>(cluster_ctarank()) : 0;
     const int rank = (PAIR == 2) ? crank : 0;      // row half of a CTA-pair tile
     const int srank = split_k ? crank : 0;         // K share of a split-K tile
@@ -368,6 +372,11 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     float* s_xchg = reinterpret_cast<float*>(smem + C::XCHG_OFF);
 
     if (threadIdx.x == 0) {
+        // the tensor maps are fetched while the barriers and TMEM are set up (they are kernel
+        // parameters, not data of the previous grid, so this may precede the dependency wait)
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        prefetch_tmap(&tmap_d);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -438,10 +447,6 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             // ------------------------------------------------------------------ TMA producer
             // The whole warp runs the loop (warp-uniform operands); one elected lane issues.
             const bool issuer = elect_one();
-            if (issuer) {
-                prefetch_tmap(&tmap_a);
-                prefetch_tmap(&tmap_b);
-            }
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;   // per-stage bits, for the abort drain
@@ -974,7 +979,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         // rounds to BF16 and stores; the second barrier keeps every CTA's shared memory alive until
         // all remote reads are done
         cluster_sync();
-        if (warp >= EPI_WARP0 && !*abort_flag) {
+        // (a masked launch covers every possible tile; clusters past the device-side count have none)
+        if (warp >= EPI_WARP0 && !*abort_flag && unit < num_tiles) {
             const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, unit, s_prefix, rank, srank);
             const int rows_per = BM / p.split;
             const int groups = rows_per * (BN / 4);
@@ -983,11 +989,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const int row = srank * rows_per + gi / (BN / 4);
                 const int c4 = (gi % (BN / 4)) * 4;
                 const uint32_t off = static_cast<uint32_t>((row * C::PSTRIDE + c4) * 4);
-                float4 sum = ld_shared_cluster_v4(mapa_shared(part_local + off, 0));
-                for (int sidx = 1; sidx < p.split; ++sidx) {
-                    const float4 v = ld_shared_cluster_v4(mapa_shared(part_local + off, sidx));
-                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-                }
+                const float4 sum = cluster_sum_v4(part_local + off, p.split);
                 if (row < ti.rows_valid && ti.n0 + c4 < p.n) {
                     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) +
                                          static_cast<size_t>(ti.d_row + row) * p.n + ti.n0 + c4;

@@ -98,6 +98,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     uint8_t* s_store = smem + C::STORE_OFF;
 
     if (threadIdx.x == 0) {
+        // the tensor maps are fetched while the barriers and TMEM are set up (they are kernel
+        // parameters, not data of the previous grid, so this may precede the dependency wait)
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        prefetch_tmap(&tmap_d);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -134,10 +139,6 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     if (warp == 0) {
         // ---------------------------------------------------------------------- TMA producer
         const bool issuer = elect_one();
-        if (issuer) {
-            prefetch_tmap(&tmap_a);
-            prefetch_tmap(&tmap_b);
-        }
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued = 0, issued_parity = 0;

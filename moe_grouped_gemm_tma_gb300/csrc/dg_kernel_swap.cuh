@@ -100,6 +100,10 @@ dg_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     float* s_xchg = reinterpret_cast<float*>(smem + C::XCHG_OFF);
 
     if (threadIdx.x == 0) {
+        // the tensor maps are fetched while the barriers and TMEM are set up (they are kernel
+        // parameters, not data of the previous grid, so this may precede the dependency wait)
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -136,10 +140,6 @@ dg_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         if (warp == 0) {
             // ------------------------------------------------------------------ TMA producer
             const bool issuer = elect_one();
-            if (issuer) {
-                prefetch_tmap(&tmap_a);
-                prefetch_tmap(&tmap_b);
-            }
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;
@@ -392,11 +392,7 @@ dg_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
                 const int col = srank * cols_per + gi % cols_per;
                 const int r4 = (gi / cols_per) * 4;
                 const uint32_t off = static_cast<uint32_t>((col * C::PSTRIDE + r4) * 4);
-                float4 sum = ld_shared_cluster_v4(mapa_shared(part_local + off, 0));
-                for (int sidx = 1; sidx < p.split; ++sidx) {
-                    const float4 v = ld_shared_cluster_v4(mapa_shared(part_local + off, sidx));
-                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-                }
+                const float4 sum = cluster_sum_v4(part_local + off, p.split);
                 const int n = ti.n0 + col;
                 if (n < p.n) {
                     __nv_bfloat16* dcol = reinterpret_cast<__nv_bfloat16*>(p.d) + n;

@@ -92,8 +92,8 @@ cudaError_t launch(const Launch& L) {
     cfg.blockDim = dim3(C::THREADS_C, 1, 1);
     cfg.dynamicSmemBytes = C::DYN_SMEM;
     cfg.stream = L.stream;
-    if (MODE == kNormal && PAIR == 1 && L.params.split > 1) {
-        // split-K: one cluster of `split` CTAs per tile, not persistent
+    if ((MODE == kNormal || MODE == kMasked) && PAIR == 1 && L.params.split > 1) {
+        // split-K: one cluster of `split` CTAs per tile (masked: per possible tile), not persistent
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(L.params.split);
         attr[0].val.clusterDim.y = 1;

@@ -317,6 +317,21 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
     return v;
 }
 
+// Sum over the cluster's CTAs 0..S-1 (S <= 8, in that order) of the float4 at the same shared-memory
+// offset in each: every remote load is issued before the first add, so the sum costs one round trip
+// through distributed shared memory instead of S.
+__device__ __forceinline__ float4 cluster_sum_v4(uint32_t local_addr, int S) {
+    float4 v[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+        if (s < S) v[s] = ld_shared_cluster_v4(mapa_shared(local_addr, static_cast<uint32_t>(s)));
+    float4 sum = v[0];
+#pragma unroll
+    for (int s = 1; s < 8; ++s)
+        if (s < S) { sum.x += v[s].x; sum.y += v[s].y; sum.z += v[s].z; sum.w += v[s].w; }
+    return sum;
+}
+
 __device__ __forceinline__ void st_global_v2(void* p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
