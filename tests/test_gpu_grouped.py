@@ -111,6 +111,18 @@ def test_masked_every_tile_shape(bn, pair, monkeypatch):
     _check_masked(c, run_masked(c), [300, 5, 129])
 
 
+@pytest.mark.parametrize("bn", [64, 128])
+@pytest.mark.parametrize("split", [2, 4, 8])
+def test_masked_split_k(bn, split, monkeypatch):
+    # clusters of `split` CTAs share a tile's K blocks; one cluster per possible tile, the ones past the
+    # device-side tile count have no work; an empty expert and rows past masked_m stay untouched
+    monkeypatch.setenv("DG_BN", str(bn))
+    monkeypatch.setenv("DG_SPLIT", str(split))
+    sizes = [300, 0, 129]
+    c = I.make_masked(I.seed_for(3, 100 + bn + split), 3, 384, 256, 1024, sizes)
+    _check_masked(c, run_masked(c), sizes)
+
+
 @pytest.mark.parametrize("G,max_m,expected_m,N,K", [
     (16, 256, 64, 4096, 7168), (4, 512, 128, 7168, 2048), (1, 1024, 256, 4096, 7168), (2, 256, 256, 7168, 2048),
 ])
