@@ -491,7 +491,7 @@ def run_ours(args):
         achieved, peak, unit, src = c.bytes / (avg_ms[dom] * 1e-3) / 1e9, bw, "GB/s", "hbm_gbs"
     roofline = {"bound": per_case[dom]["bound"], "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(c.name),
-                "kernel": f"dg_gemm_kernel, {args.workload} case {c.name}",
+                "kernel": f"{'dg_gemm_bs_kernel' if args.workload == 'ue8m0' else 'dg_gemm_kernel'}, {args.workload} case {c.name}",
                 "peak_source": f"{peak_kind} ({src})", "share": round(float(avg_ms[dom] / avg_ms.sum()), 3)}
 
     # end to end through the public API with host buffers: pinned H2D of every input, the call, D2H
