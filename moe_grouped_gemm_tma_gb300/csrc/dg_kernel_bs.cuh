@@ -61,10 +61,12 @@ struct CfgBS {
 };
 
 // Exponent byte of a power-of-two FP32 scale, replicated into the four bytes of a TMEM cell (one per
-// 32-element slice of the 128-K block); anything else is reported and its exponent used.
-__device__ __forceinline__ uint32_t ue8m0x4(float s, int* status) {
+// 32-element slice of the 128-K block). Anything else (sign, mantissa bits, zero) is flagged in `bad`,
+// which the caller reports once; its exponent is used. (A per-value branch with an atomic here made
+// the scale writers the pacing loop: 476 against 358 us on 4096 x 7168 x 16384.)
+__device__ __forceinline__ uint32_t ue8m0x4(float s, uint32_t& bad) {
     const uint32_t bits = __float_as_uint(s);
-    if ((bits & 0x807FFFFFu) != 0u || bits == 0u) atomicExch(status, STATUS_SCALE_NOT_UE8M0);
+    bad |= (bits & 0x807FFFFFu) | static_cast<uint32_t>(bits == 0u);
     return ((bits >> 23) & 0xFFu) * 0x01010101u;
 }
 
@@ -255,6 +257,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         int slot = 0, sslot = 0;
         uint32_t tphase = 0, sphase = 0;
+        uint32_t bad = 0;   // a scale that is not a power of two was seen (reported once, below)
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
             const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
@@ -270,11 +273,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                           wait_bounded(&scale_full_bar[sslot], sphase, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 const float* sl = s_scales + sslot * C::SLOT_FLOATS;
-                const uint32_t va = ue8m0x4(sl[q * 32 + lane], p.status);
+                const uint32_t va = ue8m0x4(sl[q * 32 + lane], bad);
                 const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
                 uint32_t vb[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), p.status) : 0u;
+                for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), bad) : 0u;
                 const uint32_t col = static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
                 tmem_st_x4(lane_base + col, va, va, va, va);
                 tmem_st_x8(lane_base + col + C::SFB_OFF, vb);
@@ -289,6 +292,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 if (++sslot == C::SCALE_SLOTS) { sslot = 0; sphase ^= 1u; }
             }
         }
+        if (bad != 0u) atomicExch(p.status, STATUS_SCALE_NOT_UE8M0);
     } else if (warp >= 8) {
         // ---------------------------------------------------------------------- output
         const int q = warp & 3;
