@@ -16,13 +16,15 @@
 //               tile commits the accumulator.
 //   warp 2      scale stager: per K block, cp.async copies of the block's 128 sfa values and 4 sfb
 //               block rows into a shared-memory ring (as in dg_gemm_kernel), ahead of the writers.
-//   warps 4..7  scale writers (one per TMEM lane quarter): per K block they turn the staged FP32 scales
-//               into exponents and store them with tcgen05.st into a TMEM scale slot: A's row m (lane m) in
-//               four columns (the MMA reads row m's from column m / 32), B's row n (replicated in every
-//               lane quarter, lane n % 32) in column n / 32 after them. A scale that is not a power of two
-//               is reported (DG_SCALE_NOT_UE8M0).
-//   warps 8..11 output: per tile they read the accumulator out of TMEM, release it, round to BF16 and
-//               TMA-store 32 x 16 boxes.
+//   warps 4..11 two sets of four (one warp per TMEM lane quarter in each). Set 0 writes the scales of the
+//               even K blocks (counted across tiles), set 1 those of the odd ones: each turns the staged
+//               FP32 scales into exponents and stores them with tcgen05.st into a TMEM scale slot: A's row
+//               m (lane m) in four columns (the MMA reads row m's from column m / 32), B's row n
+//               (replicated in every lane quarter, lane n % 32) in column n / 32 after them. A scale
+//               that is not a power of two is reported (DG_SCALE_NOT_UE8M0). Once a tile's scales are
+//               written, each set reads its half of the tile's columns out of the accumulator,
+//               releases it, rounds to BF16 and TMA-stores 32 x 16 boxes. (One set of writers was the
+//               pacing loop: about 930 cycles per K block against about 640 for the MMAs.)
 // Every wait is bounded as in dg_gemm_kernel.
 #pragma once
 
@@ -38,7 +40,7 @@ struct CfgBS {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int OUT_WARPS = 4;
+    static constexpr int OUT_WARPS = 8;                          // both writer/output sets
     static constexpr int STORE_BYTES = OUT_WARPS * 2048;
     static constexpr int STATIC_RESERVE = 640;
     static constexpr int SCALE_SLOTS = 16;                       // shared-memory ring of staged FP32 scales
@@ -251,13 +253,18 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             if (!ok) break;
         }
         cp_async_wait_all();
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------------- scale writers
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------------- scale writers + output
+        const int set = (warp >= 8) ? 1 : 0;
         const int q = warp & 3;
+        const int ow = warp - 4;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        int slot = 0, sslot = 0;
-        uint32_t tphase = 0, sphase = 0;
         uint32_t bad = 0;   // a scale that is not a power of two was seen (reported once, below)
+        int gbase = 0;      // K blocks of this CTA's earlier tiles: the global K-block count picks slots
+        int acc = 0;
+        uint32_t aphase = 0, store_round = 0;
+        uint8_t* wbuf = s_store + ow * 2048;
+        const int sw = (lane >> 2) & 1;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
             const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
@@ -265,7 +272,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             int bidx[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) bidx[j] = min(min(ti.n0 + 32 * j + lane, p.n - 1) / 128 - ti.n0 / 128, 3);
-            for (int kb = 0; kb < ti.nkb; ++kb) {
+            for (int kb = ((gbase & 1) == set) ? 0 : 1; kb < ti.nkb; kb += 2) {
+                const int gk = gbase + kb;
+                const int slot = gk % SLOTS, sslot = gk % C::SCALE_SLOTS;
+                const uint32_t tphase = static_cast<uint32_t>(gk / SLOTS) & 1u;
+                const uint32_t sphase = static_cast<uint32_t>(gk / C::SCALE_SLOTS) & 1u;
                 bool got = (static_cast<unsigned>(mbar_try_wait(&sf_empty_bar[slot], tphase ^ 1u)) &
                             static_cast<unsigned>(mbar_try_wait(&scale_full_bar[sslot], sphase))) != 0u;
                 if (!got)
@@ -288,39 +299,30 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     mbar_arrive(&sf_full_bar[slot]);
                     mbar_arrive(&scale_empty_bar[sslot]);
                 }
-                if (++slot == SLOTS) { slot = 0; tphase ^= 1u; }
-                if (++sslot == C::SCALE_SLOTS) { sslot = 0; sphase ^= 1u; }
             }
-        }
-        if (bad != 0u) atomicExch(p.status, STATUS_SCALE_NOT_UE8M0);
-    } else if (warp >= 8) {
-        // ---------------------------------------------------------------------- output
-        const int q = warp & 3;
-        const int ow = warp - 8;
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        int acc = 0;
-        uint32_t aphase = 0, store_round = 0;
-        uint8_t* wbuf = s_store + ow * 2048;
-        const int sw = (lane >> 2) & 1;
-        for (int t = unit; t < num_tiles; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
-            const bool got = wait_bounded(&tmem_full_bar[acc], aphase, abort_flag, p.status);
-            if (!__all_sync(0xffffffffu, got)) break;
+            gbase += ti.nkb;
+            if (!ok) break;
+
+            // this set's half of the tile: columns [set * BN/2, (set + 1) * BN/2)
+            const bool full = wait_bounded(&tmem_full_bar[acc], aphase, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, full)) break;
             tc_fence_after();
             const uint32_t taddr = lane_base + static_cast<uint32_t>(acc * BN);
             const int y = ti.m0 + q * 32;
-            constexpr int CH = BN / 16;
+            constexpr int CH = BN / 32;            // 16-column chunks per set
+            const int c0 = set * CH;
             // loads of chunk c + 1 are in flight while chunk c is rounded and staged
             uint32_t rb[2][16];
-            tmem_ld_x16(taddr, rb[0]);
+            tmem_ld_x16(taddr + c0 * 16, rb[0]);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                const int b = c & 1;
-                if (c + 1 < CH) {
+            for (int i = 0; i < CH; ++i) {
+                const int b = i & 1;
+                const int c = c0 + i;
+                if (i + 1 < CH) {
                     tmem_ld_x16(taddr + (c + 1) * 16, rb[b ^ 1]);
                 } else {
-                    // every load of the accumulator has completed: release it to the next tile's MMAs
+                    // every load of this half has completed: release it to the next tile's MMAs
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tmem_empty_bar[acc]);
@@ -345,10 +347,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     tma_store_2d(&tmap_d, half, ti.n0 + c * 16, y);
                     bulk_commit();
                 }
-                if (c + 1 < CH) tmem_ld_wait();
+                if (i + 1 < CH) tmem_ld_wait();
             }
             if (++acc == NACC) { acc = 0; aphase ^= 1u; }
         }
+        if (bad != 0u) atomicExch(p.status, STATUS_SCALE_NOT_UE8M0);
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
