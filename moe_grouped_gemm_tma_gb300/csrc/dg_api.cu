@@ -214,10 +214,12 @@ int choose_group_m(int m_blocks, int tile_m, int64_t k, const DeviceInfo& dev) {
 
 // Split-K for problems whose tiles cannot fill half the SMs (small M): a cluster of S CTAs shares a
 // tile, each CTA streaming K/S of it, so more SMs pull operands at once. Picks (BN, S in {2, 4}) with
-// the most CTAs that still fit in one wave, at least 4 K blocks per CTA; ties go to the smaller S.
+// the most CTAs that still fit in one wave, at least `min_kb` K blocks per CTA (4; the block-scaled
+// kernel, whose per-CTA set-up is longer, asks for 8: 64 x 7168 x 2048 took 22.7 us as 4 CTAs of 4
+// blocks per tile, against 14.4 us unsplit); ties go to the smaller S.
 // DG_SPLIT=<s> forces S (2, 4 or 8; 1 disables) for sweeps.
 template <size_t NC>
-int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, int kbs, int sms) {
+int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, int kbs, int sms, int min_kb = 4) {
     const char* env = getenv("DG_SPLIT");
     if (env) {
         const int s = atoi(env);
@@ -228,7 +230,7 @@ int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, i
     int best_split = 1;
     int64_t best_ctas = row_blocks * cdiv(n, sp->bn);
     for (int s = 2; s <= 4; s *= 2) {   // clusters of 8 do not all fit at once with one CTA per SM
-        if (kbs < 4 * s) break;
+        if (kbs < min_kb * s) break;
         for (size_t i = 0; i < NC; ++i) {
             const int64_t ctas = row_blocks * cdiv(n, cands[i].bn) * s;
             if (ctas <= sms && ctas > best_ctas) {
@@ -529,7 +531,8 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
     if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
 
-    const Spec sp = spec_override(kBlockScaledSpecs, choose_spec(kBlockScaledSpecs, cdiv(M, BM), N, dev.sms));
+    Spec sp = spec_override(kBlockScaledSpecs, choose_spec(kBlockScaledSpecs, cdiv(M, BM), N, dev.sms));
+    const int split = choose_split(kBlockScaledSpecs, &sp, cdiv(M, BM), N, K / 128, dev.sms, 8);
     const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
@@ -549,7 +552,7 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
     p.m_blocks = cdiv(M, BM);
     p.n_blocks = cdiv(N, bn);
     p.group_m = choose_group_m(p.m_blocks, BM, K, dev);
-    p.split = 1;
+    p.split = split;
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);

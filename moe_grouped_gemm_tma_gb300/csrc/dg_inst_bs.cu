@@ -27,18 +27,29 @@ cudaError_t launch_bs(const Launch& L) {
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::DYN_SMEM;
     cfg.stream = L.stream;
-    const int units = L.units < L.sms ? L.units : L.sms;
-    cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
-    if (units == 0) return cudaSuccess;
-    if (pdl_enabled()) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (L.params.split > 1) {
+        // split-K: one cluster of `split` CTAs per tile, not persistent
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(L.params.split);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
         cfg.numAttrs = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(L.units * L.params.split), 1, 1);
+    } else {
+        const int units = L.units < L.sms ? L.units : L.sms;
+        cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+    }
+    if (cfg.gridDim.x == 0) return cudaSuccess;
+    if (pdl_enabled()) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs += 1;
     }
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.tmap_d, L.params);
 }

@@ -57,6 +57,9 @@ struct CfgBS {
     static constexpr int SLOTS = SLOTS_FIT > 8 ? 8 : SLOTS_FIT;
     static constexpr int STORE_OFF = ((STAGES * STAGE_BYTES + SCALE_BYTES + 1023) / 1024) * 1024;
     static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
+    // split-K partial sums: [128 rows][BN + 4] FP32 in the operand ring, idle once the tile's MMAs are done
+    static constexpr int PSTRIDE = BN + 4;
+    static_assert(BM * PSTRIDE * 4 <= STAGES * STAGE_BYTES, "split-K partials must fit in the operand ring");
     static_assert(SLOTS >= 2, "at least two scale slots");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte swizzle-atom alignment");
@@ -92,8 +95,13 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int unit = static_cast<int>(blockIdx.x);
-    const int num_units = static_cast<int>(gridDim.x);
+    // split-K (few tiles): a cluster of p.split CTAs shares one tile, each CTA a K range, and the FP32
+    // partial sums are reduced through distributed shared memory (not persistent: one tile per cluster)
+    const bool split_k = p.split > 1;
+    const int srank = split_k ? static_cast<int>(cluster_ctarank()) : 0;
+    const int csize = split_k ? p.split : 1;
+    const int unit = static_cast<int>(blockIdx.x) / csize;
+    const int num_units = static_cast<int>(gridDim.x) / csize;
     const uint32_t raw = smem_u32(dyn_smem);
     uint8_t* smem = dyn_smem + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* smem_a = smem;
@@ -148,7 +156,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         uint32_t issued = 0, issued_parity = 0;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
             for (int kb = 0; kb < ti.nkb; ++kb) {
                 const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -186,7 +194,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         uint32_t last_parity = 0;
         const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
             // the tile's accumulator must have been read out by the output warps
             const bool free_acc = wait_bounded(&tmem_empty_bar[acc], aphase ^ 1u, abort_flag, p.status);
             if (!__all_sync(0xffffffffu, free_acc)) { ok = false; break; }
@@ -233,7 +241,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         int slot = 0;
         uint32_t sphase = 0;
         for (int t = unit; t < num_tiles; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
             const float* sfa_rows[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -267,7 +275,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         const int sw = (lane >> 2) & 1;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, 0);
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
             // staged sfb block row of this lane's columns n0 + 32 j + lane (columns past N reuse the last)
             int bidx[8];
 #pragma unroll
@@ -311,6 +319,26 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             const int y = ti.m0 + q * 32;
             constexpr int CH = BN / 32;            // 16-column chunks per set
             const int c0 = set * CH;
+            if (split_k) {
+                // park this CTA's FP32 partial sums (its half of the columns) in the idle operand ring;
+                // rows padded to BN + 4 floats, so the 16-byte stores of a warp hit every bank
+                float* prow = reinterpret_cast<float*>(smem) + (q * 32 + lane) * C::PSTRIDE + c0 * 16;
+#pragma unroll 1
+                for (int i = 0; i < CH; ++i) {
+                    uint32_t r[16];
+                    tmem_ld_x16(taddr + (c0 + i) * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4*>(prow + i * 16 + j) =
+                            make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tmem_empty_bar[acc]);
+                if (++acc == NACC) { acc = 0; aphase ^= 1u; }
+                continue;
+            }
             // loads of chunk c + 1 are in flight while chunk c is rounded and staged
             uint32_t rb[2][16];
             tmem_ld_x16(taddr + c0 * 16, rb[0]);
@@ -354,6 +382,31 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         if (bad != 0u) atomicExch(p.status, STATUS_SCALE_NOT_UE8M0);
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+    }
+
+    // ------------------------------------------------------------------------ split-K reduction
+    if (split_k) {
+        // every CTA's partials are visible cluster-wide after this barrier; CTA s of the cluster then
+        // reduces rows [s*128/S, (s+1)*128/S) of the tile over all S partials (fixed order s = 0..S-1),
+        // rounds to BF16 and stores; the second barrier keeps every CTA's shared memory alive until all
+        // remote reads are done
+        cluster_sync();
+        if (warp >= 4 && !*abort_flag && unit < num_tiles) {
+            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, unit, nullptr, 0, srank);
+            const int rows_per = BM / p.split;
+            const int groups = rows_per * (BN / 4);
+            const uint32_t part_local = smem_u32(smem);
+            for (int gi = static_cast<int>(threadIdx.x) - 128; gi < groups; gi += 256) {
+                const int row = srank * rows_per + gi / (BN / 4);
+                const int c4 = (gi % (BN / 4)) * 4;
+                const float4 sum = cluster_sum_v4(part_local + static_cast<uint32_t>((row * C::PSTRIDE + c4) * 4), p.split);
+                if (row < ti.rows_valid && ti.n0 + c4 < p.n) {
+                    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) + static_cast<size_t>(ti.m0 + row) * p.n + ti.n0 + c4;
+                    st_global_v2(dst, pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+                }
+            }
+        }
+        cluster_sync();
     }
 
     // ------------------------------------------------------------------------ teardown

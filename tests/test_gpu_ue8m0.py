@@ -53,3 +53,22 @@ def test_ue8m0_reports_non_power_of_two_scales():
     run_ue8m0(c.A, c.sfa, c.B, c.sfb, 128, 256)
     assert dg.dg_device_status() == 7                       # DG_SCALE_NOT_UE8M0
     assert dg.dg_device_status() == 0                       # reported once, then cleared
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("M,N,K", [(64, 1000, 3200), (100, 2112, 1024)])
+def test_ue8m0_split_k(split, M, N, K, monkeypatch):
+    # a cluster of `split` CTAs shares each tile's K blocks (unevenly when they do not divide); each
+    # accumulates its range in TMEM and the FP32 partials are reduced through distributed shared memory
+    monkeypatch.setenv("DG_SPLIT", str(split))
+    c = I.make_normal(I.seed_for(7, 50 + split + M), M, N, K, pow2=True)
+    D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
+    assert dg.dg_device_status() == 0
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 split={split} {M}x{N}x{K}")
+
+
+def test_ue8m0_split_k_reports_non_power_of_two_scales(monkeypatch):
+    monkeypatch.setenv("DG_SPLIT", "4")
+    c = I.make_normal(I.seed_for(7, 2), 64, 512, 2048)
+    run_ue8m0(c.A, c.sfa, c.B, c.sfb, 64, 512)
+    assert dg.dg_device_status() == 7
