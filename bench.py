@@ -89,8 +89,9 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(name):
-    """DRAM bytes per launch from the committed ncu record, if it was taken on the current kernels."""
+def ncu_traffic(workload, name):
+    """DRAM bytes per launch (keyed "workload:case") from the committed ncu record, if it was taken on the
+    current kernels."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -98,7 +99,7 @@ def ncu_traffic(name):
         rec = json.load(f)
     if rec.get("kernel_source_digest") != kernel_source_digest():
         return None
-    return rec.get("per_launch_bytes", {}).get(name)
+    return rec.get("per_launch_bytes", {}).get(f"{workload}:{name}")
 
 
 class ClockSampler:
@@ -490,7 +491,7 @@ def run_ours(args):
     else:
         achieved, peak, unit, src = c.bytes / (avg_ms[dom] * 1e-3) / 1e9, bw, "GB/s", "hbm_gbs"
     roofline = {"bound": per_case[dom]["bound"], "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(c.name),
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload if args.shape is None else "dense", c.name),
                 "kernel": f"{'dg_gemm_bs_kernel' if args.workload == 'ue8m0' else 'dg_gemm_kernel'}, {args.workload} case {c.name}",
                 "peak_source": f"{peak_kind} ({src})", "share": round(float(avg_ms[dom] / avg_ms.sum()), 3)}
 
