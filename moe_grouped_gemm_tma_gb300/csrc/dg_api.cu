@@ -151,6 +151,7 @@ constexpr Spec kNormalSpecs1[] = {{64, 1}, {96, 1}, {128, 1}, {160, 1}, {192, 1}
 constexpr Spec kNormalSpecs2[] = {{128, 2}, {160, 2}, {192, 2}, {224, 2}, {256, 2}};
 // block-scaled (UE8M0) normal GEMM
 constexpr Spec kBlockScaledSpecs[] = {{128, 1}, {192, 1}, {224, 1}, {256, 1}};
+constexpr Spec kBlockScaledSpecs2[] = {{128, 2}, {256, 2}};
 // B stored MN-major is staged in whole 128-column boxes
 constexpr Spec kNormalSpecsBMN[] = {{128, 1}, {256, 1}};
 constexpr Spec kContiguousSpecs[] = {{128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
@@ -531,13 +532,20 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
     if (!A || !B || !sfa || !sfb) return DG_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sfa, 4) || !aligned(sfb, 4)) return DG_MISALIGNED;
 
-    Spec sp = spec_override(kBlockScaledSpecs, choose_spec(kBlockScaledSpecs, cdiv(M, BM), N, dev.sms));
-    const int split = choose_split(kBlockScaledSpecs, &sp, cdiv(M, BM), N, K / 128, dev.sms, 8);
+    // CTA pairs halve each SM's B bytes per K block, which the block-scaled kernel (no per-block
+    // promotion loop) turns into speed: 4096 x 7168 x 16384 in 279 us against 308 us single-CTA, and
+    // faster on every M = 4096 dense shape. They are taken when the pair tiles fill at least one wave
+    // of CTAs; fewer tiles go to single-CTA tiles with split-K. DG_PAIR=1 / 2 forces the choice.
+    bool pair = M > BM && static_cast<int64_t>(cdiv(M, 2 * BM)) * cdiv(N, 256) * 2 >= dev.sms;
+    if (const char* e = getenv("DG_PAIR")) pair = (atoi(e) == 2) && M > BM;
+    Spec sp = pair ? spec_override(kBlockScaledSpecs2, choose_spec(kBlockScaledSpecs2, cdiv(M, 2 * BM), N, dev.sms))
+                   : spec_override(kBlockScaledSpecs, choose_spec(kBlockScaledSpecs, cdiv(M, BM), N, dev.sms));
+    const int split = pair ? 1 : choose_split(kBlockScaledSpecs, &sp, cdiv(M, BM), N, K / 128, dev.sms, 8);
     const int bn = sp.bn;
     Launch L;
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, M, K, BM) != DG_OK) return DG_CUDA_ERROR;
-    if (make_operand_map(&L.tmap_b, B, N, K, bn) != DG_OK) return DG_CUDA_ERROR;
+    if (make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
@@ -549,9 +557,9 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
     p.kbs = K / 128;
     p.groups = 1;
     p.sfb_rows = cdiv(N, 128);
-    p.m_blocks = cdiv(M, BM);
+    p.m_blocks = cdiv(M, BM * sp.pair);
     p.n_blocks = cdiv(N, bn);
-    p.group_m = choose_group_m(p.m_blocks, BM, K, dev);
+    p.group_m = choose_group_m(p.m_blocks, BM * sp.pair, K, dev);
     p.split = split;
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
@@ -560,11 +568,18 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
     L.sms = dev.sms;
     L.stream = stream;
     cudaError_t e = cudaErrorInvalidValue;
-    switch (bn) {
-        case 128: e = launch_bs<128>(L); break;
-        case 192: e = launch_bs<192>(L); break;
-        case 224: e = launch_bs<224>(L); break;
-        case 256: e = launch_bs<256>(L); break;
+    if (pair) {
+        switch (bn) {
+            case 128: e = launch_bs<128, 2>(L); break;
+            case 256: e = launch_bs<256, 2>(L); break;
+        }
+    } else {
+        switch (bn) {
+            case 128: e = launch_bs<128, 1>(L); break;
+            case 192: e = launch_bs<192, 1>(L); break;
+            case 224: e = launch_bs<224, 1>(L); break;
+            case 256: e = launch_bs<256, 1>(L); break;
+        }
     }
     return e == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
 }

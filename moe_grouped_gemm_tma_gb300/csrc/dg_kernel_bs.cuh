@@ -34,11 +34,13 @@ namespace dg {
 
 constexpr int STATUS_SCALE_NOT_UE8M0 = 7;   // DG_SCALE_NOT_UE8M0
 
-template <int BN>
+template <int BN, int PAIR>
 struct CfgBS {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
+    static_assert(PAIR == 1 || PAIR == 2, "PAIR is 1 or 2");
     static constexpr int A_BYTES = BM * BK;
-    static constexpr int B_BYTES = BN * BK;
+    static constexpr int B_ROWS = BN / PAIR;                      // B rows staged by each CTA
+    static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int OUT_WARPS = 8;                          // both writer/output sets
     static constexpr int STORE_BYTES = OUT_WARPS * 2048;
@@ -75,15 +77,15 @@ __device__ __forceinline__ uint32_t ue8m0x4(float s, uint32_t& bad) {
     return ((bits >> 23) & 0xFFu) * 0x01010101u;
 }
 
-template <int BN>
+template <int BN, int PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                   const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ Params p) {
-    using C = CfgBS<BN>;
+    using C = CfgBS<BN, PAIR>;
     constexpr int STAGES = C::STAGES;
     constexpr int NACC = C::NACC;
     constexpr int SLOTS = C::SLOTS;
-    constexpr uint32_t IDESC = idesc_bs_e4m3(BM, BN);
+    constexpr uint32_t IDESC = idesc_bs_e4m3(BM * PAIR, BN);
 
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
@@ -97,9 +99,14 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     const int lane = threadIdx.x & 31;
     // split-K (few tiles): a cluster of p.split CTAs shares one tile, each CTA a K range, and the FP32
     // partial sums are reduced through distributed shared memory (not persistent: one tile per cluster)
-    const bool split_k = p.split > 1;
-    const int srank = split_k ? static_cast<int>(cluster_ctarank()) : 0;
-    const int csize = split_k ? p.split : 1;
+    // CTA pairs (cta_group::2, 256-row tiles): each CTA stages its 128 A rows and half of B's rows;
+    // the leader issues the MMAs; both CTAs write their own scale slots and store their own rows
+    const bool split_k = PAIR == 1 && p.split > 1;
+    const int crank = (PAIR == 2 || split_k) ? static_cast<int>(cluster_ctarank()) : 0;
+    const int rank = (PAIR == 2) ? crank : 0;
+    const bool leader = (rank == 0);
+    const int srank = split_k ? crank : 0;
+    const int csize = (PAIR == 2) ? 2 : (split_k ? p.split : 1);
     const int unit = static_cast<int>(blockIdx.x) / csize;
     const int num_units = static_cast<int>(gridDim.x) / csize;
     const uint32_t raw = smem_u32(dyn_smem);
@@ -121,10 +128,10 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(&tmem_full_bar[a], 1);
-            mbar_init(&tmem_empty_bar[a], C::OUT_WARPS);
+            mbar_init(&tmem_empty_bar[a], C::OUT_WARPS * PAIR);
         }
         for (int s = 0; s < SLOTS; ++s) {
-            mbar_init(&sf_full_bar[s], 4);
+            mbar_init(&sf_full_bar[s], 4 * PAIR);
             mbar_init(&sf_empty_bar[s], 1);
         }
         for (int s = 0; s < C::SCALE_SLOTS; ++s) {
@@ -135,13 +142,18 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&s_tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR == 2) {
+            tmem_alloc_pair(&s_tmem_base, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&s_tmem_base, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     grid_dependency_wait();
     grid_launch_dependents();
     tc_fence_before();
-    __syncthreads();
+    if (PAIR == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = s_tmem_base;
@@ -156,15 +168,22 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         uint32_t issued = 0, issued_parity = 0;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
+            const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
             for (int kb = 0; kb < ti.nkb; ++kb) {
                 const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 if (issuer) {
                     const int x = (ti.kb0 + kb) * BK;
-                    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
-                    tma_load_2d(&tmap_a, &full_bar[stage], smem_a + stage * C::A_BYTES, x, ti.a_row);
-                    tma_load_2d(&tmap_b, &full_bar[stage], smem_b + stage * C::B_BYTES, x, ti.b_row);
+                    if (PAIR == 1 || leader) {
+                        mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
+                        tma_load_2d(&tmap_a, &full_bar[stage], smem_a + stage * C::A_BYTES, x, ti.a_row);
+                        tma_load_2d(&tmap_b, &full_bar[stage], smem_b + stage * C::B_BYTES, x, ti.b_row);
+                    } else {
+                        // the peer's halves complete on the leader's barrier
+                        const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                        tma_load_2d_pair(&tmap_a, bar, smem_a + stage * C::A_BYTES, x, ti.a_row);
+                        tma_load_2d_pair(&tmap_b, bar, smem_b + stage * C::B_BYTES, x, ti.b_row);
+                    }
                 }
                 __syncwarp();
                 issued |= 1u << stage;
@@ -180,11 +199,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        if (!ok && issuer) {
+        if (!ok && (PAIR == 1 || leader) && issuer) {
             for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s)) drain_wait(&full_bar[s], (issued_parity >> s) & 1u);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && leader) {
         // ---------------------------------------------------------------------- MMA issuer
         const bool issuer = elect_one();
         int stage = 0, slot = 0, acc = 0;
@@ -194,7 +213,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         uint32_t last_parity = 0;
         const uint32_t a_base = smem_u32(smem_a), b_base = smem_u32(smem_b);
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
+            const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
             // the tile's accumulator must have been read out by the output warps
             const bool free_acc = wait_bounded(&tmem_empty_bar[acc], aphase ^ 1u, abort_flag, p.status);
             if (!__all_sync(0xffffffffu, free_acc)) { ok = false; break; }
@@ -215,20 +234,29 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         // 32-element slice k of the block: scale byte k of every cell
-                        mma_f8f6f4_bs(d_tmem, a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4)),
-                                      b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4)),
-                                      IDESC | IDESC_BS_SFA(k) | IDESC_BS_SFB(k), sfa_t, sfb_t,
-                                      (kb > 0 || k > 0) ? 1u : 0u);
+                        const uint64_t ad = a_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
+                        const uint64_t bd = b_desc + static_cast<uint64_t>(k * (UMMA_K >> 4));
+                        const uint32_t id = IDESC | IDESC_BS_SFA(k) | IDESC_BS_SFB(k);
+                        if (PAIR == 2) mma_f8f6f4_bs_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+                        else mma_f8f6f4_bs(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(&empty_bar[stage]);
-                    mma_commit(&sf_empty_bar[slot]);
+                    if (PAIR == 2) {
+                        mma_commit_pair(&empty_bar[stage], 0x3);
+                        mma_commit_pair(&sf_empty_bar[slot], 0x3);
+                    } else {
+                        mma_commit(&empty_bar[stage]);
+                        mma_commit(&sf_empty_bar[slot]);
+                    }
                 }
                 __syncwarp();
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 if (++slot == SLOTS) { slot = 0; sphase ^= 1u; }
             }
             if (!ok) break;
-            if (issuer) mma_commit(&tmem_full_bar[acc]);
+            if (issuer) {
+                if (PAIR == 2) mma_commit_pair(&tmem_full_bar[acc], 0x3);
+                else mma_commit(&tmem_full_bar[acc]);
+            }
             __syncwarp();
             any = true;
             last_acc = acc;
@@ -241,7 +269,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         int slot = 0;
         uint32_t sphase = 0;
         for (int t = unit; t < num_tiles; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
+            const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
             const float* sfa_rows[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -275,7 +303,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         const int sw = (lane >> 2) & 1;
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, t, nullptr, 0, srank);
+            const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
             // staged sfb block row of this lane's columns n0 + 32 j + lane (columns past N reuse the last)
             int bidx[8];
 #pragma unroll
@@ -298,13 +326,17 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
 #pragma unroll
                 for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), bad) : 0u;
                 const uint32_t col = static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
-                tmem_st_x4(lane_base + col, va, va, va, va);
+                // A's exponent in the slot's first eight columns: the MMA reads row m's from column m / 32
+                // (of the CTA's own rows, or of the pair's 256)
+                const uint32_t va8[8] = {va, va, va, va, va, va, va, va};
+                tmem_st_x8(lane_base + col, va8);
                 tmem_st_x8(lane_base + col + C::SFB_OFF, vb);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&sf_full_bar[slot]);
+                    if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&sf_full_bar[slot]), 0));
+                    else mbar_arrive(&sf_full_bar[slot]);
                     mbar_arrive(&scale_empty_bar[sslot]);
                 }
             }
@@ -350,10 +382,14 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 if (i + 1 < CH) {
                     tmem_ld_x16(taddr + (c + 1) * 16, rb[b ^ 1]);
                 } else {
-                    // every load of this half has completed: release it to the next tile's MMAs
+                    // every load of this half has completed: release it to the next tile's MMAs (on the
+                    // leader's barrier for a pair)
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tmem_empty_bar[acc]);
+                    if (lane == 0) {
+                        if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
+                        else mbar_arrive(&tmem_empty_bar[acc]);
+                    }
                 }
                 uint8_t* half = wbuf + (store_round & 1u) * 1024;
                 ++store_round;
@@ -392,7 +428,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         // remote reads are done
         cluster_sync();
         if (warp >= 4 && !*abort_flag && unit < num_tiles) {
-            const TileInfo ti = decode_tile<kNormal, BN, 1>(p, unit, nullptr, 0, srank);
+            const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, unit, nullptr, rank, srank);
             const int rows_per = BM / p.split;
             const int groups = rows_per * (BN / 4);
             const uint32_t part_local = smem_u32(smem);
@@ -411,10 +447,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
 
     // ------------------------------------------------------------------------ teardown
     tc_fence_before();
-    __syncthreads();
+    if (PAIR == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

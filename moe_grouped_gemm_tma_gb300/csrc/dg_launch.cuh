@@ -25,7 +25,7 @@ template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L);
 
 // The block-scaled (UE8M0) normal GEMM (dg_inst_bs.cu).
-template <int BN>
+template <int BN, int PAIR>
 cudaError_t launch_bs(const Launch& L);
 
 // The swapped-operand normal GEMM for few rows (dg_inst_swap.cu).

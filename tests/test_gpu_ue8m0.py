@@ -72,3 +72,30 @@ def test_ue8m0_split_k_reports_non_power_of_two_scales(monkeypatch):
     c = I.make_normal(I.seed_for(7, 2), 64, 512, 2048)
     run_ue8m0(c.A, c.sfa, c.B, c.sfb, 64, 512)
     assert dg.dg_device_status() == 7
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(200, 1000, 768), (520, 4096, 2048), (256, 264, 384)])
+def test_ue8m0_cta_pairs(M, N, K, bn, monkeypatch):
+    # 256-row tiles over a CTA pair (cta_group::2): each CTA writes the exponents of its own rows and all
+    # of B's; ragged M leaves the second CTA of the last pair partly or wholly past M
+    monkeypatch.setenv("DG_PAIR", "2")
+    monkeypatch.setenv("DG_BN", str(bn))
+    c = I.make_normal(I.seed_for(7, 70 + bn + M), M, N, K, pow2=True)
+    D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
+    assert dg.dg_device_status() == 0
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 pair BN={bn} {M}x{N}x{K}")
+
+
+def test_ue8m0_cta_pairs_integer_exact_bitwise(monkeypatch):
+    monkeypatch.setenv("DG_PAIR", "2")
+    rng = np.random.default_rng(17)
+    M, N, K = 512, 384, 512
+    codes = np.array([0xB8, 0x00, 0x38], dtype=np.uint8)
+    A = torch.from_numpy(rng.choice(codes, size=(M, K)))
+    B = torch.from_numpy(rng.choice(codes, size=(N, K)))
+    sfa = torch.from_numpy(np.ldexp(1.0, rng.integers(-2, 3, size=(M, K // 128))).astype(np.float32))
+    sfb = torch.from_numpy(np.ldexp(1.0, rng.integers(-2, 3, size=(N // 128, K // 128))).astype(np.float32))
+    D = run_ue8m0(A, sfa, B, sfb, M, N)
+    assert dg.dg_device_status() == 0
+    np.testing.assert_array_equal(bf16_bits(D), O.gemm_fp8_nt(A, sfa, B, sfb))
