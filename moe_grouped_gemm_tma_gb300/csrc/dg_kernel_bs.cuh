@@ -25,6 +25,11 @@
 //               written, each set reads its half of the tile's columns out of the accumulator,
 //               releases it, rounds to BF16 and TMA-stores 32 x 16 boxes. (One set of writers was the
 //               pacing loop: about 930 cycles per K block against about 640 for the MMAs.)
+// CTA pairs (PAIR = 2): a cluster of two CTAs computes a 256-row tile with cta_group::2 MMAs issued by
+// the leader. Each CTA stages its 128 A rows and half of B's rows (the peer's loads complete on the
+// leader's barrier), writes the exponents of its own A rows and of all of B's rows into its own TMEM
+// slot (the MMA reads both CTAs' slots at the same address), and reads out and stores its own rows;
+// the peer's slot and accumulator releases arrive on the leader's barriers.
 // Every wait is bounded as in dg_gemm_kernel.
 #pragma once
 
