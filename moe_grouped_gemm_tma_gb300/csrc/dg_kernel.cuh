@@ -30,8 +30,10 @@
 //               FMA), then releases the scale slot. Wide tiles: the warpgroups split the BN columns.
 //               Narrow tiles (BN <= 64): each warpgroup takes every other K block over all columns,
 //               and the two partial sums are exchanged once per tile through shared memory. At the
-//               end of a tile they round to BF16 and TMA-store 32 x 16 boxes, or TMA-add 32 x 8 FP32
-//               boxes into the weight gradient.
+//               end of a tile they round to BF16 and either stage the whole tile in shared memory for
+//               TMA stores that complete in the background (where that fits beside a four-stage ring)
+//               or write it with coalesced plain stores; the weight gradient is TMA-added in 32 x 8
+//               FP32 boxes.
 // The MMA of K block kb+1.. overlaps the promotion of block kb (NACC accumulators in flight), and the
 // store of one tile overlaps the first MMAs of the next. Small-M GEMMs split K over a cluster of CTAs
 // and reduce the FP32 partials through distributed shared memory.
@@ -844,7 +846,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 // D[g] += tile: FP32 boxes of 32 rows x 8 columns, added element-wise by the TMA (one
                 // add per element, so the result does not depend on timing), or stored (overwriting
                 // form); the three-dimensional map [G][M][N] skips rows past M and columns past N
-                uint8_t* wbuf = s_store + ew * (C::STORE_SLOTS * 1024);
+                uint8_t* wbuf = s_store + ew * C::STORE_WARP_BYTES;
                 const int y = ti.m0 + q * 32;
                 const int sw = (lane >> 2) & 1;
 #pragma unroll
