@@ -51,3 +51,20 @@ def test_single_rank_passthrough_and_job_throughput():
     assert bench.max_over_ranks(3.25, 1, torch.device("cpu")) == 3.25
     # 2 replicas x 10 steps x 1 TFLOP in 2 s (2000 ms) = 10 TFLOP/s for the whole job
     assert bench.job_tflops(1e12, 10, 2, 2000.0) == pytest.approx(10.0)
+
+
+def test_traffic_record_matches_current_kernels_only(monkeypatch):
+    # roofline.traffic comes from the committed ncu record only while it was taken on the current
+    # kernel source, and is keyed by workload and case (the dense and UE8M0 workloads share case names)
+    import json
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    assert rec["kernel_source_digest"] == bench.kernel_source_digest(), "profiles/traffic.json is stale"
+    for key in rec["per_launch_bytes"]:
+        workload, case = key.split(":", 1)
+        assert workload in bench.WORKLOADS, key
+        assert bench.ncu_traffic(workload, case) == rec["per_launch_bytes"][key]
+    assert bench.ncu_traffic("dense", "4096x7168x16384") != bench.ncu_traffic("ue8m0", "4096x7168x16384")
+    assert bench.ncu_traffic("dense", "no such case") is None
+    # after any change to the kernel sources the record no longer applies
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda: "0" * 16)
+    assert bench.ncu_traffic("dense", "4096x7168x16384") is None
