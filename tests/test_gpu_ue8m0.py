@@ -99,3 +99,18 @@ def test_ue8m0_cta_pairs_integer_exact_bitwise(monkeypatch):
     D = run_ue8m0(A, sfa, B, sfb, M, N)
     assert dg.dg_device_status() == 0
     np.testing.assert_array_equal(bf16_bits(D), O.gemm_fp8_nt(A, sfa, B, sfb))
+
+
+@pytest.mark.parametrize("N,K", [(2112, 7168), (24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048)])
+def test_ue8m0_workload_sampled_rows(N, K):
+    # the block-scaled workload at full size (M in {64, 128, 4096}: split-K clusters for few rows, CTA
+    # pairs for M = 4096), as the bench runs it; the oracle recomputes a sample of rows
+    from tests.gpu_util import sample_rows
+    big = I.make_normal(I.seed_for(1, 0), 4096, N, K, pow2=True)
+    for M in (64, 128, 4096):
+        A, sfa = big.A[:M], big.sfa[:M]
+        D = run_ue8m0(A, sfa, big.B, big.sfb, M, N)
+        assert dg.dg_device_status() == 0
+        rows = sample_rows(M, 24, seed=M + N + K)
+        want = O.gemm_fp8_nt(A, sfa, big.B, big.sfb, rows=rows)
+        check_bf16(bf16_bits(D)[rows], want, f"ue8m0 {M}x{N}x{K}")
