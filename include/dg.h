@@ -83,6 +83,18 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
                                int M, int N, int K, cudaStream_t stream);
 
 /*
+ * The same block-scaled GEMM with the scales already in the packed UE8M0 format (pages: the SM100
+ * scale layout, four UE8M0 values in one int32):
+ *   sfa  [M, ceil(K/512)] int32          sfb  [ceil(N/128), ceil(K/512)] int32
+ * Byte j (least significant first) of word w of a row is the biased exponent e of K block 4w + j; the
+ * scale it stands for is 2^(e - 127). Bytes past the last K block are ignored. The exponents are used
+ * as they are (no check; e = 255 is not a number). Result as dg_gemm_fp8_nt with those scales.
+ * Device pointers, 4-byte aligned; errors as dg_gemm_fp8_nt.
+ */
+dg_status dg_gemm_fp8_nt_ue8m0_packed(const uint8_t* A, const int32_t* sfa, const uint8_t* B, const int32_t* sfb,
+                                      void* D, int M, int N, int K, cudaStream_t stream);
+
+/*
  * m-grouped GEMM, contiguous layout (pages: m_grouped_gemm_fp8_fp8_bf16_nt_contiguous; for training
  * forward and inference prefill). The experts' token rows are stacked along M; each expert's segment
  * starts on a multiple of 128 rows (segments padded to 128).

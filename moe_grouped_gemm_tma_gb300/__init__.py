@@ -17,7 +17,8 @@ import os
 import threading
 
 __all__ = [
-    "DGError", "load", "dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
+    "DGError", "load", "dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_gemm_fp8_nt_ue8m0_packed",
+    "dg_m_grouped_contiguous", "dg_m_grouped_masked",
     "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status", "dg_status_string", "scale_shapes", "library_path",
 ]
 
@@ -54,6 +55,7 @@ def load(build_if_missing: bool = True):
             L.dg_gemm_fp8_nt.argtypes = [P, P, P, P, P, I, I, I, P]
             L.dg_gemm_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
             L.dg_gemm_fp8_nt_ue8m0.argtypes = [P, P, P, P, P, I, I, I, P]
+            L.dg_gemm_fp8_nt_ue8m0_packed.argtypes = [P, P, P, P, P, I, I, I, P]
             L.dg_m_grouped_contiguous.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
             L.dg_m_grouped_masked.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
             L.dg_k_grouped_wgrad.argtypes = [P, P, P, P, P, P, I, I, I, P]
@@ -61,7 +63,8 @@ def load(build_if_missing: bool = True):
             L.dg_device_status.argtypes = [P]
             L.dg_status_string.argtypes = [I]
             L.dg_status_string.restype = ctypes.c_char_p
-            for f in ("dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_m_grouped_contiguous", "dg_m_grouped_masked",
+            for f in ("dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_gemm_fp8_nt_ue8m0_packed",
+                      "dg_m_grouped_contiguous", "dg_m_grouped_masked",
                       "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status"):
                 getattr(L, f).restype = I
             _lib = L
@@ -174,6 +177,28 @@ def dg_gemm_fp8_nt_ue8m0(A, sfa, B, sfb, D, stream=None):
         raise ValueError(f"scale shapes {tuple(sfa.shape)}, {tuple(sfb.shape)} != {scale_shapes(M, N, K)}")
     st = load().dg_gemm_fp8_nt_ue8m0(_ptr(A), _ptr(sfa), _ptr(B), _ptr(sfb), _ptr(D), M, N, K, _stream(stream))
     _check(st, "dg_gemm_fp8_nt_ue8m0")
+    return D
+
+
+def dg_gemm_fp8_nt_ue8m0_packed(A, sfa, B, sfb, D, stream=None):
+    """The block-scaled GEMM with packed UE8M0 scales: sfa int32 [M, ceil(K/512)], sfb int32
+    [ceil(N/128), ceil(K/512)], byte j of word w = biased exponent of K block 4w + j."""
+    torch = _torch()
+    A, B = _codes(A, "A"), _codes(B, "B")
+    sfa, sfb, D = _dense(sfa, "sfa"), _dense(sfb, "sfb"), _dense(D, "D")
+    if sfa.dtype != torch.int32 or sfb.dtype != torch.int32:
+        raise TypeError("packed scales must be int32")
+    if D.dtype != torch.bfloat16:
+        raise TypeError("D must be bfloat16")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)} B {tuple(B.shape)} D {tuple(D.shape)}")
+    words = (K // 128 + 3) // 4
+    if tuple(sfa.shape) != (M, words) or tuple(sfb.shape) != ((N + 127) // 128, words):
+        raise ValueError(f"packed scale shapes {tuple(sfa.shape)}, {tuple(sfb.shape)} != {(M, words)}, {((N + 127) // 128, words)}")
+    st = load().dg_gemm_fp8_nt_ue8m0_packed(_ptr(A), _ptr(sfa), _ptr(B), _ptr(sfb), _ptr(D), M, N, K, _stream(stream))
+    _check(st, "dg_gemm_fp8_nt_ue8m0_packed")
     return D
 
 

@@ -517,8 +517,10 @@ dg_status dg_gemm_fp8(const uint8_t* A, const float* sfa, const uint8_t* B, cons
     return gemm_impl(A, sfa, B, sfb, D, M, N, K, a_mn_major != 0, b_mn_major != 0, stream);
 }
 
-dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
-                               int M, int N, int K, cudaStream_t stream) {
+// The block-scaled GEMM behind both UE8M0 entry points: FP32 power-of-two scales (converted and checked
+// on the device) or packed UE8M0 exponents (four K blocks per int32, used as they are).
+static dg_status ue8m0_impl(const uint8_t* A, const void* sfa, const uint8_t* B, const void* sfb, void* D,
+                            int M, int N, int K, bool packed, cudaStream_t stream) {
     if (M < 0 || N < 0 || K < 0) return DG_INVALID_ARG;
     if (M == 0 || N == 0) return DG_OK;
     if (!D) return DG_INVALID_ARG;
@@ -548,8 +550,10 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
     if (make_operand_map(&L.tmap_b, B, N, K, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
     if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
-    p.sfa = sfa;
-    p.sfb = sfb;
+    p.sfa = static_cast<const float*>(sfa);
+    p.sfb = static_cast<const float*>(sfb);
+    p.sf_packed = packed ? 1 : 0;
+    p.sf_words = cdiv(K / 128, 4);
     p.d = D;
     p.status = dev.status;
     p.rows = M;
@@ -582,6 +586,16 @@ dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t
         }
     }
     return e == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+}
+
+dg_status dg_gemm_fp8_nt_ue8m0(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb, void* D,
+                               int M, int N, int K, cudaStream_t stream) {
+    return ue8m0_impl(A, sfa, B, sfb, D, M, N, K, false, stream);
+}
+
+dg_status dg_gemm_fp8_nt_ue8m0_packed(const uint8_t* A, const int32_t* sfa, const uint8_t* B, const int32_t* sfb,
+                                      void* D, int M, int N, int K, cudaStream_t stream) {
+    return ue8m0_impl(A, sfa, B, sfb, D, M, N, K, true, stream);
 }
 
 dg_status dg_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_t* B, const float* sfb,

@@ -91,6 +91,8 @@ struct Params {
     int group_m;               // normal / contiguous: row blocks per raster band (row block fastest)
     int overwrite;             // k-grouped: store the tile (D = ...) instead of adding it (D += ...)
     int a_mn, b_mn;            // normal layout: A stored [K, M] / B stored [K, N] (MN-major operands)
+    int sf_packed;             // block-scaled: sfa / sfb hold UE8M0 exponents, four K blocks per int32
+    int sf_words;              // block-scaled, packed: int32 words per scale row, ceil(kbs / 4)
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 

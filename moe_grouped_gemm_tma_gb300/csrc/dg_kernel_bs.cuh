@@ -21,7 +21,8 @@
 //               FP32 scales into exponents and stores them with tcgen05.st into a TMEM scale slot: A's row
 //               m (lane m) in four columns (the MMA reads row m's from column m / 32), B's row n
 //               (replicated in every lane quarter, lane n % 32) in column n / 32 after them. A scale
-//               that is not a power of two is reported (DG_SCALE_NOT_UE8M0). Once a tile's scales are
+//               that is not a power of two is reported (DG_SCALE_NOT_UE8M0); packed UE8M0 input (four
+//               exponent bytes per 32-bit word) is used as it is. Once a tile's scales are
 //               written, each set reads its half of the tile's columns out of the accumulator,
 //               releases it, rounds to BF16 and TMA-stores 32 x 16 boxes. (One set of writers was the
 //               pacing loop: about 930 cycles per K block against about 640 for the MMAs.)
@@ -275,19 +276,23 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         uint32_t sphase = 0;
         for (int t = unit; t < num_tiles; t += num_units) {
             const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
+            // FP32 scales: one value per K block; packed UE8M0: the 32-bit word holding the block's
+            // exponent (the writers pick its byte)
+            const int row_stride = p.sf_packed ? p.sf_words : p.kbs;
             const float* sfa_rows[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                sfa_rows[i] = p.sfa + static_cast<size_t>(min(ti.a_row + lane + 32 * i, p.rows - 1)) * p.kbs + ti.kb0;
-            const float* sfb_src = p.sfb + static_cast<size_t>(min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1)) * p.kbs + ti.kb0;
+                sfa_rows[i] = p.sfa + static_cast<size_t>(min(ti.a_row + lane + 32 * i, p.rows - 1)) * row_stride;
+            const float* sfb_src = p.sfb + static_cast<size_t>(min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1)) * row_stride;
             bool ok = true;
             for (int kb = 0; kb < ti.nkb; ++kb) {
                 const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 float* dst = s_scales + slot * C::SLOT_FLOATS;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + kb);
-                if (lane < 4) cp_async_4(dst + BM + lane, sfb_src + kb);
+                const int kidx = p.sf_packed ? ((ti.kb0 + kb) >> 2) : (ti.kb0 + kb);
+                for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + kidx);
+                if (lane < 4) cp_async_4(dst + BM + lane, sfb_src + kidx);
                 cp_async_arrive_noinc(&scale_full_bar[slot]);
                 if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
             }
@@ -325,11 +330,20 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                           wait_bounded(&scale_full_bar[sslot], sphase, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 const float* sl = s_scales + sslot * C::SLOT_FLOATS;
-                const uint32_t va = ue8m0x4(sl[q * 32 + lane], bad);
                 const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
-                uint32_t vb[8];
+                uint32_t va, vb[8];
+                if (p.sf_packed) {
+                    // byte (K block mod 4) of the staged words, replicated into the cell's four bytes
+                    const uint32_t sh = 8u * static_cast<uint32_t>((ti.kb0 + kb) & 3);
+                    va = ((__float_as_uint(sl[q * 32 + lane]) >> sh) & 0xFFu) * 0x01010101u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), bad) : 0u;
+                    for (int j = 0; j < 8; ++j)
+                        vb[j] = (j < BN / 32) ? ((__float_as_uint(pick4(b4, bidx[j])) >> sh) & 0xFFu) * 0x01010101u : 0u;
+                } else {
+                    va = ue8m0x4(sl[q * 32 + lane], bad);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), bad) : 0u;
+                }
                 const uint32_t col = static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
                 // A's exponent in the slot's first eight columns: the MMA reads row m's from column m / 32
                 // (of the CTA's own rows, or of the pair's 256)

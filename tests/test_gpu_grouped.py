@@ -210,3 +210,27 @@ def test_dense_wgrad_k_zero():
                        accumulate=False)
     assert dg.dg_device_status() == 0
     assert bool((D == 0.0).all())          # the empty product, stored
+
+
+def test_masked_replayed_from_a_cuda_graph():
+    # decode runs the masked layout under CUDA graphs: one capture, replayed with new per-expert counts
+    # written into the same device buffer; every argument the host sees stays fixed
+    G, max_m, N, K = 4, 256, 1024, 512
+    first = [100, 0, 256, 37]
+    c = I.make_masked(I.seed_for(3, 900), G, max_m, N, K, first, 128)
+    dA, dsfa, dB, dsfb = dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb)
+    mm = dev(c.masked_m)
+    D = sentinel_bf16(G, max_m, N)
+    dg.dg_m_grouped_masked(dA, dsfa, dB, dsfb, mm, D, expected_m=128)   # one-time set-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dg.dg_m_grouped_masked(dA, dsfa, dB, dsfb, mm, D, expected_m=128)
+    for sizes in (first, [1, 255, 0, 129], [256, 256, 256, 256]):
+        mm.copy_(torch.tensor(sizes, dtype=torch.int32))
+        D.view(torch.int16).fill_(SENTINEL - 65536)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert dg.dg_device_status() == 0
+        c2 = I.MaskedCase(c.G, c.max_m, c.N, c.K, 128, c.A, c.sfa, c.B, c.sfb, torch.tensor(sizes, dtype=torch.int32))
+        _check_masked(c2, bf16_bits(D).reshape(G * max_m, N), sizes)

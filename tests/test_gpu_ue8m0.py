@@ -114,3 +114,43 @@ def test_ue8m0_workload_sampled_rows(N, K):
         rows = sample_rows(M, 24, seed=M + N + K)
         want = O.gemm_fp8_nt(A, sfa, big.B, big.sfb, rows=rows)
         check_bf16(bf16_bits(D)[rows], want, f"ue8m0 {M}x{N}x{K}")
+
+
+def pack_ue8m0(sf):
+    """FP32 power-of-two scales [rows, kbs] -> packed UE8M0 int32 [rows, ceil(kbs/4)] (byte j of word w =
+    biased exponent of block 4w + j); unused trailing bytes are 0xEE, which the kernel must ignore."""
+    sf = sf.contiguous().numpy()
+    rows, kbs = sf.shape
+    words = (kbs + 3) // 4
+    e = np.full((rows, words * 4), 0xEE, dtype=np.uint8)
+    bits = sf.view(np.uint32)
+    assert ((bits & 0x807FFFFF) == 0).all()
+    e[:, :kbs] = (bits >> 23).astype(np.uint8)
+    return torch.from_numpy(e.view(np.int32).reshape(rows, words).copy())
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 128), (200, 1000, 640), (129, 2112, 1408), (64, 4096, 7168),
+                                   (520, 264, 896), (4096, 2112, 1536)])
+def test_ue8m0_packed_matches_fp32_scales_bitwise(M, N, K):
+    # the packed format carries the same exponents, so the two entry points run the same tensor-core
+    # arithmetic: bit-identical outputs, and the oracle agrees within the tolerance
+    c = I.make_normal(I.seed_for(7, 500 + M + N + K), M, N, K, pow2=True)
+    D_f32 = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
+    assert dg.dg_device_status() == 0
+    D_pk = sentinel_bf16(M, N)
+    dg.dg_gemm_fp8_nt_ue8m0_packed(dev(c.A), dev(pack_ue8m0(c.sfa)), dev(c.B), dev(pack_ue8m0(c.sfb)), D_pk)
+    assert dg.dg_device_status() == 0
+    np.testing.assert_array_equal(bf16_bits(D_pk), bf16_bits(D_f32))
+    rows = np.unique(np.linspace(0, M - 1, min(M, 48)).astype(int))
+    want = O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb, rows=rows)
+    check_bf16(bf16_bits(D_pk)[rows], want, f"ue8m0 packed {M}x{N}x{K}")
+
+
+def test_ue8m0_packed_rejects_wrong_shapes():
+    c = I.make_normal(I.seed_for(7, 3), 128, 256, 640, pow2=True)
+    D = sentinel_bf16(128, 256)
+    with pytest.raises(ValueError):
+        dg.dg_gemm_fp8_nt_ue8m0_packed(dev(c.A), dev(pack_ue8m0(c.sfa))[:, :1].contiguous(), dev(c.B),
+                                       dev(pack_ue8m0(c.sfb)), D)
+    with pytest.raises(TypeError):
+        dg.dg_gemm_fp8_nt_ue8m0_packed(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), D)
