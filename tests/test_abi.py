@@ -21,7 +21,8 @@ def declared_symbols():
 def test_header_declares_every_operation():
     syms = declared_symbols()
     for s in ("dg_gemm_fp8_nt", "dg_m_grouped_contiguous", "dg_m_grouped_masked", "dg_k_grouped_wgrad",
-              "dg_wgrad_fp8_nt", "dg_status_string", "dg_device_status"):
+              "dg_wgrad_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_gemm_fp8_nt_ue8m0_packed",
+              "dg_status_string", "dg_device_status"):
         assert s in syms
 
 
@@ -73,6 +74,13 @@ def test_rejects_bad_shapes_before_any_cuda_call():
     assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, ok, -1, 8, 128, 1, None) == 1
     assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, ok, 8, 8, 0, 1, None) == 0          # K = 0, accumulate: no-op
     assert L.dg_wgrad_fp8_nt(ok, ok, ok, ok, _fake(0x10008), 8, 8, 0, 0, None) == 3  # zeroing misaligned D
+    for f in (L.dg_gemm_fp8_nt_ue8m0, L.dg_gemm_fp8_nt_ue8m0_packed):
+        assert f(ok, ok, ok, ok, ok, -1, 8, 128, None) == 1
+        assert f(ok, ok, ok, ok, ok, 0, 8, 128, None) == 0                       # empty: no-op
+        assert f(ok, ok, ok, ok, ok, 4, 8, 100, None) == 2                       # K % 128
+        assert f(ok, ok, ok, ok, ok, 4, 12, 128, None) == 2                      # N % 8
+        assert f(ok, ok, ok, ok, _fake(0x10008), 4, 8, 128, None) == 3           # D misaligned
+        assert f(ok, ok, ok, ok, None, 4, 8, 128, None) == 1
 
 
 def test_scale_shapes_follow_the_pages_usage_example():
