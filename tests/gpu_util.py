@@ -73,3 +73,16 @@ def sample_rows(total, count, seed, must=()):
     if extra:
         rows.update(int(x) for x in rng.choice(total, size=min(extra, total), replace=False))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def pack_ue8m0(sf):
+    """FP32 power-of-two scales [rows, kbs] -> packed UE8M0 int32 [rows, ceil(kbs/4)] (byte j of word w =
+    biased exponent of block 4w + j); unused trailing bytes are 0xEE, which the kernel must ignore."""
+    sf = sf.contiguous().numpy()
+    rows, kbs = sf.shape
+    words = (kbs + 3) // 4
+    e = np.full((rows, words * 4), 0xEE, dtype=np.uint8)
+    bits = sf.view(np.uint32)
+    assert ((bits & 0x807FFFFF) == 0).all()
+    e[:, :kbs] = (bits >> 23).astype(np.uint8)
+    return torch.from_numpy(e.view(np.int32).reshape(rows, words).copy())

@@ -8,7 +8,7 @@ import torch
 import moe_grouped_gemm_tma_gb300 as dg
 from moe_grouped_gemm_tma_gb300 import inputs as I
 from oracle import oracle as O
-from tests.gpu_util import bf16_bits, check_bf16, dev, sentinel_bf16
+from tests.gpu_util import bf16_bits, check_bf16, dev, pack_ue8m0, sentinel_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -114,19 +114,6 @@ def test_ue8m0_workload_sampled_rows(N, K):
         rows = sample_rows(M, 24, seed=M + N + K)
         want = O.gemm_fp8_nt(A, sfa, big.B, big.sfb, rows=rows)
         check_bf16(bf16_bits(D)[rows], want, f"ue8m0 {M}x{N}x{K}")
-
-
-def pack_ue8m0(sf):
-    """FP32 power-of-two scales [rows, kbs] -> packed UE8M0 int32 [rows, ceil(kbs/4)] (byte j of word w =
-    biased exponent of block 4w + j); unused trailing bytes are 0xEE, which the kernel must ignore."""
-    sf = sf.contiguous().numpy()
-    rows, kbs = sf.shape
-    words = (kbs + 3) // 4
-    e = np.full((rows, words * 4), 0xEE, dtype=np.uint8)
-    bits = sf.view(np.uint32)
-    assert ((bits & 0x807FFFFF) == 0).all()
-    e[:, :kbs] = (bits >> 23).astype(np.uint8)
-    return torch.from_numpy(e.view(np.int32).reshape(rows, words).copy())
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 128), (200, 1000, 640), (129, 2112, 1408), (64, 4096, 7168),
