@@ -128,24 +128,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        busy = sorted(sm)[len(sm) // 2:] if sm else []
-        return {"sm_mhz": float(np.median(busy)) if busy else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(text):
+    """Clock record of a timed region from nvidia-smi CSV lines (ClockSampler.FIELDS, no header, no
+    units): the median SM clock over the busier half of the samples (the sampler starts and stops a
+    little outside the region), the maximum SM clock, and every throttle reason seen active. Lines that
+    do not parse (fewer fields, "[N/A]") are skipped."""
+    sm, smax, reasons = [], [], set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for line in text.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            smax.append(float(parts[1]))
+        except ValueError:
+            continue
+        for name, v in zip(names, parts[4:8]):
+            if v.lower() == "active":
+                reasons.add(name)
+    busy = sorted(sm)[len(sm) // 2:] if sm else []
+    return {"sm_mhz": float(np.median(busy)) if busy else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def dist_env():

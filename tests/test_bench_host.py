@@ -69,3 +69,46 @@ def test_traffic_record_matches_current_kernels_only(monkeypatch):
     # after any change to the kernel sources the record no longer applies
     monkeypatch.setattr(bench, "kernel_source_digest", lambda: "0" * 16)
     assert bench.ncu_traffic("dense", "4096x7168x16384") is None
+
+
+# nvidia-smi lines as the sampler asks for them: sm, max sm, power, active mask, hw_slowdown,
+# hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+_IDLE = "1980, 2070, 300.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"
+_BUSY = "2070, 2070, 1100.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"
+_CAPPED = "1995, 2070, 1398.7, 0x0000000000000004, Not Active, Not Active, Not Active, Active"
+_HOT = "1500, 2070, 1200.0, 0x0000000000000040, Not Active, Active, Not Active, Not Active"
+
+
+def test_clock_record_median_of_the_busy_half_and_reasons():
+    rec = bench.parse_clock_samples("\n".join([_IDLE, _BUSY, _BUSY, _CAPPED, _BUSY, _IDLE]) + "\n")
+    # sorted 1980 1980 1995 2070 2070 2070: the busier half is 2070 x 3
+    assert rec == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 6}
+    rec = bench.parse_clock_samples("\n".join([_HOT, _BUSY, _CAPPED, _BUSY]))
+    assert rec["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert rec["sm_mhz"] == pytest.approx(2070.0)
+
+
+def test_clock_record_skips_unparsable_lines_and_reports_no_samples():
+    rec = bench.parse_clock_samples("[N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]\nshort, line\n" + _BUSY)
+    assert rec["samples"] == 1 and rec["sm_mhz"] == 2070.0 and rec["reasons"] == []
+    assert bench.parse_clock_samples("") == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_clock_sampler_stop_reads_its_process_output():
+    class FakeProc:
+        def __init__(self, text):
+            self.text, self.terminated = text, False
+
+        def terminate(self):
+            self.terminated = True
+
+        def communicate(self, timeout=None):
+            return self.text, None
+
+    sampler = bench.ClockSampler.__new__(bench.ClockSampler)
+    sampler.proc = FakeProc("\n".join([_CAPPED, _BUSY, _BUSY]))
+    rec = sampler.stop()
+    assert sampler.proc.terminated
+    assert rec["samples"] == 3 and rec["sm_mhz"] == 2070.0 and rec["reasons"] == ["sw_power_cap"]
+    sampler.proc = None
+    assert sampler.stop()["reasons"] == ["nvidia-smi unavailable"]
