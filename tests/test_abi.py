@@ -87,3 +87,45 @@ def test_scale_shapes_follow_the_pages_usage_example():
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "page_usage_example.json")))
     sfa, sfb = dg.scale_shapes(g["M"], g["N"], g["K"])
     assert list(sfa) == g["sfa_shape"] and list(sfb) == g["sfb_shape"]
+
+
+def test_grouped_entry_points_check_arguments_before_any_cuda_call():
+    L = dg.load()
+    ok, odd16, odd4 = _fake(0x10000), _fake(0x10008), _fake(0x10002)
+    # contiguous: (A, sfa, B, sfb, m_indices, D, Mt, N, K, G)
+    C = L.dg_m_grouped_contiguous
+    assert C(ok, ok, ok, ok, ok, ok, 0, 8, 128, 2, None) == 0           # no rows: no-op
+    assert C(ok, ok, ok, ok, ok, ok, 128, 0, 128, 2, None) == 0         # no columns: no-op
+    assert C(ok, ok, ok, ok, ok, ok, 128, 8, 128, -1, None) == 1
+    assert C(ok, ok, ok, ok, ok, ok, 128, 8, 0, 2, None) == 2           # K = 0 has no expert product
+    assert C(ok, ok, ok, ok, ok, ok, 128, 12, 128, 2, None) == 2        # N % 8
+    assert C(ok, ok, ok, ok, None, ok, 128, 8, 128, 2, None) == 1       # no m_indices
+    assert C(odd16, ok, ok, ok, ok, ok, 128, 8, 128, 2, None) == 3      # A not 16-byte aligned
+    assert C(ok, odd4, ok, ok, ok, ok, 128, 8, 128, 2, None) == 3       # sfa not 4-byte aligned
+    assert C(ok, ok, ok, ok, odd4, ok, 128, 8, 128, 2, None) == 3       # m_indices not 4-byte aligned
+    # masked: (A, sfa, B, sfb, masked_m, D, G, max_m, N, K, expected_m)
+    Mk = L.dg_m_grouped_masked
+    assert Mk(ok, ok, ok, ok, ok, ok, 0, 64, 8, 128, 0, None) == 0      # no experts: no-op
+    assert Mk(ok, ok, ok, ok, ok, ok, 2, 0, 8, 128, 0, None) == 0       # no rows: no-op
+    assert Mk(ok, ok, ok, ok, ok, ok, 2, -1, 8, 128, 0, None) == 1
+    assert Mk(ok, ok, ok, ok, ok, ok, 1025, 64, 8, 128, 0, None) == 1   # above the 1024-expert limit
+    assert Mk(ok, ok, ok, ok, ok, ok, 2, 64, 8, 0, 0, None) == 2
+    assert Mk(ok, ok, ok, ok, ok, ok, 2, 64, 12, 128, 0, None) == 2
+    assert Mk(ok, ok, ok, ok, None, ok, 2, 64, 8, 128, 0, None) == 1    # no masked_m
+    assert Mk(ok, ok, ok, ok, ok, odd16, 2, 64, 8, 128, 0, None) == 3   # D not 16-byte aligned
+    assert Mk(ok, ok, ok, ok, odd4, ok, 2, 64, 8, 128, 0, None) == 3    # masked_m not 4-byte aligned
+    assert Mk(ok, ok, ok, ok, ok, ok, 2, 1 << 30, 8, 128, 0, None) == 2  # G * max_m rows beyond int32
+    # k-grouped: (A, sfa, B, sfb, ks_host, D, G, M, N)
+    K = L.dg_k_grouped_wgrad
+    ks2 = (ctypes.c_int32 * 2)(128, 256)
+    assert K(ok, ok, ok, ok, ks2, ok, 2, 0, 8, None) == 0               # no rows: no-op
+    assert K(ok, ok, ok, ok, ks2, ok, -1, 8, 8, None) == 1
+    assert K(ok, ok, ok, ok, None, ok, 2, 8, 8, None) == 1              # no ks
+    assert K(ok, ok, ok, ok, (ctypes.c_int32 * 129)(*([128] * 129)), ok, 129, 8, 8, None) == 1  # above 128 experts
+    assert K(ok, ok, ok, ok, ks2, ok, 2, 8, 12, None) == 2              # N % 8
+    assert K(None, ok, ok, ok, ks2, ok, 2, 8, 8, None) == 1             # no A
+    assert K(ok, ok, ok, odd4, ks2, ok, 2, 8, 8, None) == 3             # sfb not 4-byte aligned
+    assert K(ok, ok, ok, ok, ks2, odd16, 2, 8, 8, None) == 3            # D not 16-byte aligned
+    big = (ctypes.c_int32 * 2)((1 << 31) - 128, (1 << 31) - 128)
+    assert K(ok, ok, ok, ok, big, ok, 2, 8, 8, None) == 2               # sum of ks beyond int32
+    assert K(ok, ok, ok, ok, ks2, ok, 2, 1 << 30, 8, None) == 2         # G * M beyond int32
