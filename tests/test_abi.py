@@ -129,3 +129,32 @@ def test_grouped_entry_points_check_arguments_before_any_cuda_call():
     big = (ctypes.c_int32 * 2)((1 << 31) - 128, (1 << 31) - 128)
     assert K(ok, ok, ok, ok, big, ok, 2, 8, 8, None) == 2               # sum of ks beyond int32
     assert K(ok, ok, ok, ok, ks2, ok, 2, 1 << 30, 8, None) == 2         # G * M beyond int32
+
+
+def test_binding_has_no_cpu_path():
+    # host tensors are refused before the library is called: there is no CPU fallback
+    import torch
+    from moe_grouped_gemm_tma_gb300 import inputs as I
+    c = I.make_normal(I.seed_for(0), 128, 256, 512)
+    D = torch.empty(128, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dg.dg_gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb, D)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dg.dg_gemm_fp8_nt_ue8m0(c.A, c.sfa, c.B, c.sfb, D)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dg.dg_wgrad_fp8_nt(c.A, c.sfa, c.A, c.sfa, torch.zeros(128, 128))
+    with pytest.raises(TypeError, match="e4m3 codes"):
+        dg.dg_gemm_fp8_nt(c.A.float(), c.sfa, c.B, c.sfb, D)
+
+
+def test_package_never_imports_the_oracle():
+    # the product path (binding, build, input generators) does not reach the test oracle
+    pkg = os.path.join(ROOT, "moe_grouped_gemm_tma_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", text, flags=re.M), f
+                assert "liboracle" not in text and "oracle.cpp" not in text, f
