@@ -38,7 +38,7 @@ def _worker(rank, world, port, results):
 
 def test_two_rank_reduction_and_rank0_rule():
     world = 2
-    results = mp.Manager().dict()
+    results = mp.get_context("spawn").Manager().dict()   # no fork of this multi-threaded process
     mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
     for rank in range(world):
         slowest, ref_rc, env = results[rank]
