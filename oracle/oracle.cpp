@@ -67,7 +67,8 @@ uint16_t bf16_bits(double x) {
     int e2;
     std::frexp(a, &e2);                     // a in [2^(e2-1), 2^e2)
     int q = std::max(e2 - 1, -126) - 7;
-    double r = std::nearbyint(std::ldexp(a, -q));   // default rounding mode: to nearest, ties even
+    double r = (ORACLE_PLANT == 10) ? std::trunc(std::ldexp(a, -q))
+                                    : std::nearbyint(std::ldexp(a, -q));   // default rounding mode: to nearest, ties even
     if (r >= 256.0) { r = 128.0; q += 1; }
     if (q + 7 > 127) return sign | 0x7F80;  // overflow to infinity
     const uint32_t ri = static_cast<uint32_t>(r);
@@ -96,8 +97,13 @@ void row_sums(const uint8_t* a_row, const float* sfa_row, const uint8_t* B, cons
         double acc = 0.0;
         for (int64_t kb = kb0; kb < kb1 - (ORACLE_PLANT == 2); ++kb) {
             double p = 0.0;   // exact: see the header
+#if ORACLE_PLANT == 12
+            for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) p += a_dec[k] * tab[B[k * N + n]];
+#else
             for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) p += a_dec[k] * tab[b_row[k]];
-            const double s = static_cast<double>(sfa_row[kb]) * static_cast<double>(sfb_row[kb]);
+#endif
+            const int64_t skb = (ORACLE_PLANT == 14) ? kb0 : kb;
+            const double s = static_cast<double>(sfa_row[skb]) * static_cast<double>(sfb_row[skb]);
             acc += (ORACLE_PLANT == 5 && kb % 2) ? -s * p : s * p;
         }
         out[n] = acc;
@@ -136,7 +142,8 @@ int oracle_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, con
     parallel_rows(n_rows, n_threads, [&](int64_t i) {
         const int64_t m = rows ? rows[i] : i;
         std::vector<double> a_dec(K), acc(N);
-        row_sums(A + m * K, sfa + m * kbs, B, sfb, N, K, kbs, 0, kbs, false, a_dec, acc.data());
+        const int64_t sfa_r = (ORACLE_PLANT == 9) ? (m / 128) * 128 : m;
+        row_sums(A + m * K, sfa + sfa_r * kbs, B, sfb, N, K, kbs, 0, kbs, false, a_dec, acc.data());
         for (int64_t n = 0; n < N; ++n) D[i * N + n] = oracle_bf16_bits(acc[n]);
     });
     return 0;
@@ -152,7 +159,7 @@ int oracle_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_
     if (!rows) n_rows = Mt;
     parallel_rows(n_rows, n_threads, [&](int64_t i) {
         const int64_t r = rows ? rows[i] : i;
-        const int64_t g = (ORACLE_PLANT == 8) ? 0 : m_indices[r];
+        const int64_t g = (ORACLE_PLANT == 8 || (ORACLE_PLANT == 13 && m_indices[r] < 0)) ? 0 : m_indices[r];
         if (g < 0 || g >= G) return;
         std::vector<double> a_dec(K), acc(N);
         row_sums(A + r * K, sfa + r * kbs, B + g * N * K, sfb + g * nb * kbs, N, K, kbs, 0, kbs, false,
@@ -199,7 +206,8 @@ int oracle_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* B,
         std::vector<double> a_dec(std::max<int64_t>(sumK, 1)), acc(N);
         int64_t koff = 0;
         for (int64_t g = 0; g < G; ++g) {
-            const int64_t kb0 = koff / 128, kb1 = (koff + ks[g]) / 128;
+            const int64_t late = (ORACLE_PLANT == 11 && ks[g] > 0 && (koff + ks[g]) / 128 < kbs) ? 1 : 0;
+            const int64_t kb0 = koff / 128 + late, kb1 = (koff + ks[g]) / 128 + late;
             row_sums(A + m * sumK, sfa + m * kbs, B, sfb, N, sumK, kbs, kb0, kb1, true, a_dec, acc.data());
             float* drow = D + (g * n_rows + i) * N;
             for (int64_t n = 0; n < N; ++n)

@@ -24,6 +24,12 @@ PLANTS = {
     6: "wgrad sfb taken per 128-row block instead of per row",
     7: "masked layout writes row masked_m",
     8: "contiguous layout ignores the group of the row",
+    9: "sfa taken per 128-row block instead of per row",
+    10: "BF16 rounding truncates toward zero",
+    11: "k-grouped expert windows start one K block late",
+    12: "B read as [K, N] instead of [N, K]",
+    13: "contiguous padding rows (group -1) computed as group 0",
+    14: "every K block scaled by the first block's scales",
 }
 
 PINS = [
@@ -35,6 +41,7 @@ PINS = [
     P.test_worked_example_closed_form,
     P.test_pow2_scaling_of_sfb_block_row_scales_its_128_columns_exactly,
     P.test_contiguous_bruteforce_small,
+    P.test_contiguous_equals_per_group_normal_and_skips_padding,
     P.test_masked_equals_per_group_normal_and_leaves_rows_untouched,
     P.test_kgrouped_bruteforce_with_accumulation,
     P.test_kgrouped_g1_equals_dense_definition,
