@@ -158,3 +158,15 @@ def test_package_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", text, flags=re.M), f
                 assert "liboracle" not in text and "oracle.cpp" not in text, f
+
+
+def test_sources_name_no_batched_copy_call():
+    # batched host<->device copy calls are closed for this library: every copy is one plain async copy
+    # (the pattern is assembled from parts so that this file does not name them either)
+    pat = re.compile("(cuda|cu)Memcpy(3D)?" + "Batch" + "Async")
+    for dirpath, dirs, files in os.walk(ROOT):
+        dirs[:] = [d for d in dirs if d not in (".git", "_work", "gpurun_out", "_build", "__pycache__")]
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp", ".c", ".sh")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8", errors="replace").read()
+                assert not pat.search(text), os.path.join(dirpath, f)
