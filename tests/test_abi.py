@@ -170,3 +170,12 @@ def test_sources_name_no_batched_copy_call():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp", ".c", ".sh")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8", errors="replace").read()
                 assert not pat.search(text), os.path.join(dirpath, f)
+
+
+def test_kernels_report_failures_without_trapping():
+    # a kernel that gives up records a status word and returns: no trap and no device-side assert
+    csrc = os.path.join(ROOT, "moe_grouped_gemm_tma_gb300", "csrc")
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        assert "__trap" not in text and not re.search(r"\btrap\s*;", text), f
+        assert not re.search(r"(?<!static_)\bassert\s*\(", text), f
