@@ -179,3 +179,31 @@ def test_kernels_report_failures_without_trapping():
         text = open(os.path.join(csrc, f), encoding="utf-8").read()
         assert "__trap" not in text and not re.search(r"\btrap\s*;", text), f
         assert not re.search(r"(?<!static_)\bassert\s*\(", text), f
+
+
+def test_every_device_loop_without_a_counted_bound_is_a_known_bounded_one():
+    # Waits in the kernels end: wait_bounded gives up after a time limit and raises the abort flag,
+    # drain_wait gives up after a shorter one; the only other open loops are the masked layout's binary
+    # search (hi - lo halves each pass) and the host-side stage count. A new open loop must be added
+    # here deliberately, with its bound.
+    known = {
+        "while (s > 1 && 1024 + ((s * stage_bytes + scale_bytes + 1023) / 1024) * 1024 + store_bytes + static_bytes > SMEM_LIMIT)",
+        "while (hi - lo > 1) {",
+        "while (true) {",                              # wait_bounded: exits on success, abort or time limit
+        "while (!mbar_try_wait(bar, parity))",         # drain_wait: exits on success or time limit
+    }
+    csrc = os.path.join(ROOT, "moe_grouped_gemm_tma_gb300", "csrc")
+    found = []
+    for f in sorted(os.listdir(csrc)):
+        for line in open(os.path.join(csrc, f), encoding="utf-8"):
+            code = line.split("//")[0].strip()
+            if re.search(r"\bwhile\s*\(|\bfor\s*\(\s*;\s*;", code):
+                found.append((f, code))
+    assert found, "no loops found: the scan is broken"
+    for f, code in found:
+        assert code in known, (f, code)
+    text = open(os.path.join(csrc, "dg_kernel.cuh"), encoding="utf-8").read()
+    body = text[text.index("bool wait_bounded("):text.index("void drain_wait(")]
+    assert "WAIT_LIMIT_NS" in body and "abort_flag" in body
+    body = text[text.index("void drain_wait("):]
+    assert "DRAIN_LIMIT_NS" in body[:400]
