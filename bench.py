@@ -66,7 +66,7 @@ WORKLOADS = {
                  "U[0.5,1.5] x 4096 padded to 128, (M,N) in {(7168,4096),(2048,7168)}"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-CPU_SAMPLE_ROWS = 64      # cpu_baseline: rows per case
+CPU_SAMPLE_ROWS = 1024    # cpu_baseline: rows per case (all rows of a smaller case); ~10 s on 16 host cores
 STREAM_COPY_BYTES = 256 << 20   # per-case in-stream timing: input copies cycled per case (2 x L2)
 REF_SAMPLE_ROWS = 16      # --impl reference: rows per case per step
 
@@ -217,7 +217,8 @@ def dense_cases(only=None, pow2=False):
             f"{M}x{N}x{K}", 2.0 * M * N * K, M * K + N * K + 4 * M * kb + 4 * nb * kb + 2 * M * N, inp, (M, N),
             torch.bfloat16,
             lambda d, o, s: dg.dg_gemm_fp8_nt(d["A"], d["sfa"], d["B"], d["sfb"], o, stream=s),
-            lambda h, r: (O.gemm_fp8_nt(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"]), 2.0 * r * h["B"].shape[0] * h["B"].shape[1])[1]))
+            lambda h, r: (O.gemm_fp8_nt(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"]),
+                          2.0 * min(r, h["A"].shape[0]) * h["B"].shape[0] * h["B"].shape[1])[1]))
     return cases
 
 
@@ -240,9 +241,9 @@ def layouts_cases():
                 (M, N), torch.bfloat16,
                 (lambda a, b: lambda d, o, s: dg.dg_gemm_fp8(d["A"], d["sfa"], d["B"], d["sfb"], o, a_mn_major=a,
                                                               b_mn_major=b, stream=s))(a_mn, b_mn),
-                (lambda a, b: lambda h, r: (O.gemm_fp8_nt((h["A"].t() if a else h["A"])[:r].contiguous(), h["sfa"][:r],
-                                                          (h["B"].t() if b else h["B"]).contiguous(), h["sfb"]),
-                                            2.0 * r * N * K)[1])(a_mn, b_mn)))
+                (lambda a, b, n_, k_: lambda h, r: (O.gemm_fp8_nt((h["A"].t() if a else h["A"])[:r].contiguous(), h["sfa"][:r],
+                                                                  (h["B"].t() if b else h["B"]).contiguous(), h["sfb"]),
+                                                    2.0 * min(r, M) * n_ * k_)[1])(a_mn, b_mn, N, K)))
     return cases
 
 
@@ -312,8 +313,8 @@ def kgrouped_cases():
                 (M + N) * sumK + 4 * (M + N) * sumK // 128 + 8 * G * M * N, inp, (G, M, N), torch.float32,
                 (lambda ks_: lambda d, o, s: dg.dg_k_grouped_wgrad(d["A"], d["sfa"], d["B"], d["sfb"], ks_, o, stream=s))(ks),
                 (lambda ks_: lambda h, r: (O.k_grouped_wgrad(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], ks_,
-                                                            np.zeros((len(ks_), r, h["B"].shape[0]), np.float32)),
-                                           2.0 * r * h["B"].shape[0] * sum(ks_))[1])(ks),
+                                                            np.zeros((len(ks_), min(r, h["A"].shape[0]), h["B"].shape[0]), np.float32)),
+                                           2.0 * min(r, h["A"].shape[0]) * h["B"].shape[0] * sum(ks_))[1])(ks),
                 init_out=c.D_in))
     return cases
 
@@ -581,7 +582,7 @@ def run_ours(args):
                                  "ms_stream from back-to-back launches of one case on distinct buffer copies"},
             "roofline": roofline,
             "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"first {CPU_SAMPLE_ROWS} rows of each of the {n} cases "
+                             "sample": f"first {CPU_SAMPLE_ROWS} rows (all rows of a smaller case) of each of the {n} cases "
                                        f"({cpu_fl / 1e9:.1f} GFLOP in {cpu_s:.1f} s)"},
             "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,

@@ -112,3 +112,19 @@ def test_clock_sampler_stop_reads_its_process_output():
     assert rec["samples"] == 3 and rec["sm_mhz"] == 2070.0 and rec["reasons"] == ["sw_power_cap"]
     sampler.proc = None
     assert sampler.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+@pytest.mark.parametrize("workload", ["dense", "layouts"])
+def test_cpu_baseline_counts_each_cases_own_flops(workload, monkeypatch):
+    # the oracle legs report 2 * rows * N * K for the rows they computed, each case with its own N and K
+    # (the oracle call itself is stubbed out: only the count is checked here)
+    from oracle import oracle as O
+    monkeypatch.setattr(O, "gemm_fp8_nt", lambda *a, **k: None)
+    cases = bench.build_cases(workload)
+    assert len(cases) == 18
+    for c in cases:
+        M, N, K = (int(x) for x in c.name.split()[-1].split("x"))
+        host = {k: v for k, v in c.inputs.items()}
+        for r in (16, 100, 5000):
+            assert c.oracle(host, r) == 2.0 * min(r, M) * N * K, (c.name, r)
+        assert c.flops == 2.0 * M * N * K
