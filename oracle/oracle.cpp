@@ -28,12 +28,6 @@
 #include <thread>
 #include <vector>
 
-// ORACLE_PLANT selects a deliberately wrong variant, used only by the test that checks the pins
-// catch plausible mistakes; the oracle proper is built with ORACLE_PLANT = 0.
-#ifndef ORACLE_PLANT
-#define ORACLE_PLANT 0
-#endif
-
 namespace {
 
 // OCP 8-bit floating point, E4M3 ("fn" variant, as torch.float8_e4m3fn): sign bit 7, exponent bits
@@ -45,7 +39,7 @@ double e4m3_value(uint8_t code) {
     const int f = code & 0x7;
     if (e == 15 && f == 7) return std::nan("");
     const double mag = (e == 0) ? std::ldexp(static_cast<double>(f), -9)
-                                : std::ldexp(static_cast<double>(8 + f), e - 10 - (ORACLE_PLANT == 3));  // (1 + f/8) 2^(e-7)
+                                : std::ldexp(static_cast<double>(8 + f), e - 10);  // (1 + f/8) 2^(e-7)
     return s ? -mag : mag;
 }
 
@@ -67,8 +61,7 @@ uint16_t bf16_bits(double x) {
     int e2;
     std::frexp(a, &e2);                     // a in [2^(e2-1), 2^e2)
     int q = std::max(e2 - 1, -126) - 7;
-    double r = (ORACLE_PLANT == 10) ? std::trunc(std::ldexp(a, -q))
-                                    : std::nearbyint(std::ldexp(a, -q));   // default rounding mode: to nearest, ties even
+    double r = std::nearbyint(std::ldexp(a, -q));   // default rounding mode: to nearest, ties even
     if (r >= 256.0) { r = 128.0; q += 1; }
     if (q + 7 > 127) return sign | 0x7F80;  // overflow to infinity
     const uint32_t ri = static_cast<uint32_t>(r);
@@ -87,24 +80,13 @@ void row_sums(const uint8_t* a_row, const float* sfa_row, const uint8_t* B, cons
     for (int64_t k = kb0 * 128; k < kb1 * 128; ++k) a_dec[k] = tab[a_row[k]];
     for (int64_t n = 0; n < N; ++n) {
         const uint8_t* b_row = B + n * K;
-#if ORACLE_PLANT == 1
-        const float* sfb_row = sfb + (per_col_sfb ? n : n / 64 % ((N + 127) / 128)) * kbs;
-#elif ORACLE_PLANT == 6
-        const float* sfb_row = sfb + (n / 128) * kbs;
-#else
         const float* sfb_row = sfb + (per_col_sfb ? n : n / 128) * kbs;
-#endif
         double acc = 0.0;
-        for (int64_t kb = kb0; kb < kb1 - (ORACLE_PLANT == 2); ++kb) {
+        for (int64_t kb = kb0; kb < kb1; ++kb) {
             double p = 0.0;   // exact: see the header
-#if ORACLE_PLANT == 12
-            for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) p += a_dec[k] * tab[B[k * N + n]];
-#else
             for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) p += a_dec[k] * tab[b_row[k]];
-#endif
-            const int64_t skb = (ORACLE_PLANT == 14) ? kb0 : kb;
-            const double s = static_cast<double>(sfa_row[skb]) * static_cast<double>(sfb_row[skb]);
-            acc += (ORACLE_PLANT == 5 && kb % 2) ? -s * p : s * p;
+            const double s = static_cast<double>(sfa_row[kb]) * static_cast<double>(sfb_row[kb]);
+            acc += s * p;
         }
         out[n] = acc;
     }
@@ -127,7 +109,7 @@ extern "C" {
 double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
 
 uint16_t oracle_bf16_bits(double x) {
-    return ORACLE_PLANT == 4 ? bf16_bits(static_cast<float>(x)) : bf16_bits(x);
+    return bf16_bits(x);
 }
 
 int oracle_hardware_threads(void) { return static_cast<int>(std::thread::hardware_concurrency()); }
@@ -142,8 +124,7 @@ int oracle_gemm_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, con
     parallel_rows(n_rows, n_threads, [&](int64_t i) {
         const int64_t m = rows ? rows[i] : i;
         std::vector<double> a_dec(K), acc(N);
-        const int64_t sfa_r = (ORACLE_PLANT == 9) ? (m / 128) * 128 : m;
-        row_sums(A + m * K, sfa + sfa_r * kbs, B, sfb, N, K, kbs, 0, kbs, false, a_dec, acc.data());
+        row_sums(A + m * K, sfa + m * kbs, B, sfb, N, K, kbs, 0, kbs, false, a_dec, acc.data());
         for (int64_t n = 0; n < N; ++n) D[i * N + n] = oracle_bf16_bits(acc[n]);
     });
     return 0;
@@ -159,7 +140,7 @@ int oracle_m_grouped_contiguous(const uint8_t* A, const float* sfa, const uint8_
     if (!rows) n_rows = Mt;
     parallel_rows(n_rows, n_threads, [&](int64_t i) {
         const int64_t r = rows ? rows[i] : i;
-        const int64_t g = (ORACLE_PLANT == 8 || (ORACLE_PLANT == 13 && m_indices[r] < 0)) ? 0 : m_indices[r];
+        const int64_t g = m_indices[r];
         if (g < 0 || g >= G) return;
         std::vector<double> a_dec(K), acc(N);
         row_sums(A + r * K, sfa + r * kbs, B + g * N * K, sfb + g * nb * kbs, N, K, kbs, 0, kbs, false,
@@ -181,7 +162,7 @@ int oracle_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t* B
         const int64_t gr = rows ? rows[i] : i;
         const int64_t g = gr / max_m, r = gr % max_m;
         const int64_t lim = std::min<int64_t>(std::max<int32_t>(masked_m[g], 0), max_m);
-        if (r >= lim + (ORACLE_PLANT == 7)) return;
+        if (r >= lim) return;
         std::vector<double> a_dec(K), acc(N);
         row_sums(A + gr * K, sfa + gr * kbs, B + g * N * K, sfb + g * nb * kbs, N, K, kbs, 0, kbs, false,
                  a_dec, acc.data());
@@ -206,8 +187,7 @@ int oracle_k_grouped_wgrad(const uint8_t* A, const float* sfa, const uint8_t* B,
         std::vector<double> a_dec(std::max<int64_t>(sumK, 1)), acc(N);
         int64_t koff = 0;
         for (int64_t g = 0; g < G; ++g) {
-            const int64_t late = (ORACLE_PLANT == 11 && ks[g] > 0 && (koff + ks[g]) / 128 < kbs) ? 1 : 0;
-            const int64_t kb0 = koff / 128 + late, kb1 = (koff + ks[g]) / 128 + late;
+            const int64_t kb0 = koff / 128, kb1 = (koff + ks[g]) / 128;
             row_sums(A + m * sumK, sfa + m * kbs, B, sfb, N, sumK, kbs, kb0, kb1, true, a_dec, acc.data());
             float* drow = D + (g * n_rows + i) * N;
             for (int64_t n = 0; n < N; ++n)
