@@ -1,11 +1,15 @@
 #!/usr/bin/env python
 """Throughput of the block-scaled FP8 GEMM and its MoE variants, printed as one JSON line.
 
-Workloads (--workload; one "step" = every case of the workload once, each on its own device buffers):
+With no --workload, every workload below runs in turn; the line's top-level numbers are the dense
+workload's (the headline configuration) and `per_workload` holds each workload's own value, roofline,
+e2e, clocks, CPU baseline and per-case figures. One "step" = every case of a workload once, each on its
+own device buffers.
 
-* dense (default): the normal FP8 GEMM NT, D[M,N] = A[M,K] . B[N,K]^T, 1x128 / 128x128 FP32 block
+* dense (headline): the normal FP8 GEMM NT, D[M,N] = A[M,K] . B[N,K]^T, 1x128 / 128x128 FP32 block
   scales, BF16 out, for M in {64, 128, 4096} x (N, K) in {(2112, 7168), (24576, 1536), (32768, 512),
   (7168, 16384), (4096, 7168), (7168, 2048)}: 18 GEMMs, about 1.5 GB of buffers in all.
+* tiny: the parity-sized normal GEMM, M=128, N=256, K=512 (launch-bound; reported for completeness).
 * contiguous: m-grouped contiguous layout, G in {4, 8} experts, rows per expert U[0.7, 1.3] x {8192,
   4096} padded to 128, (N, K) in {(4096, 7168), (7168, 2048)}.
 * masked: m-grouped masked layout (decode), G in {1, 2, 4, 16}, (max_m, expected_m) in {(256, 64),
@@ -24,12 +28,15 @@ value: TFLOP/s over the whole step (2MNK per case, real rows only), summed over 
        is excluded.
 e2e:   the same through the public API with host buffers: pinned host -> device copies of every case's
        inputs, the call, and the device -> host copy of every output inside the timed region.
-roofline: the case with the largest share of the step, against the measured tensor peak (FP8 = 2 x the
-       measured sustained BF16 rate) or HBM peak, whichever bounds it (per_case lists all cases).
+roofline: the case with the largest share of the step, against the measured peak that bounds it: the
+       FP8 tensor peak = 2 x the measured burst BF16 rate (the kernels are timed launch by launch, well
+       under a second), or the measured HBM copy rate. `frac_of_sustained` restates it against 2 x the
+       sustained BF16 rate. per_case lists every case against the same peaks.
 cpu_baseline / --impl reference: the CPU oracle on a bounded row sample of the same cases.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--workload W] [--impl reference]; for N > 1
 under torch.distributed.run, one replica per rank (the GEMMs are independent; there is no exchange).
+--timed-only runs the warm-up and timed steps alone (for profiler captures).
 """
 from __future__ import annotations
 
@@ -51,7 +58,10 @@ if ROOT not in sys.path:
 METRIC = "FP8 GEMM TFLOP/s per shape on 1 GB300; fraction of min(FP8 peak, HBM roofline)"
 MS = (64, 128, 4096)
 NKS = ((2112, 7168), (24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048))
+HEADLINE = "dense"
+WORKLOAD_ORDER = ("dense", "tiny", "contiguous", "masked", "kgrouped", "layouts", "ue8m0")
 WORKLOADS = {
+    "tiny": "parity-sized normal FP8 GEMM NT, M=128, N=256, K=512, BF16 out",
     "dense": ("dense normal FP8 GEMM NT (e4m3, 1x128 / 128x128 FP32 scales, BF16 out), M in {64,128,4096} x "
               "(N,K) in {(2112,7168),(24576,1536),(32768,512),(7168,16384),(4096,7168),(7168,2048)}"),
     "contiguous": ("m-grouped contiguous FP8 GEMM (MoE prefill / training forward), G in {4,8}, rows per expert "
@@ -66,7 +76,8 @@ WORKLOADS = {
                  "U[0.5,1.5] x 4096 padded to 128, (M,N) in {(7168,4096),(2048,7168)}"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-CPU_SAMPLE_ROWS = 1024    # cpu_baseline: rows per case (all rows of a smaller case); ~10 s on 16 host cores
+CPU_SAMPLE_ROWS = 1024    # cpu_baseline of the headline: rows per case (all rows of a smaller case); ~10 s on 16 cores
+CPU_SAMPLE_ROWS_OTHER = 128   # ... of every other workload (a few seconds each)
 STREAM_COPY_BYTES = 256 << 20   # per-case in-stream timing: input copies cycled per case (2 x L2)
 REF_SAMPLE_ROWS = 16      # --impl reference: rows per case per step
 
@@ -199,7 +210,7 @@ def ue8m0_cases():
     return cases
 
 
-def dense_cases(only=None, pow2=False):
+def dense_cases(only=None, pow2=False, seed_config=1):
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
     from oracle import oracle as O
@@ -207,7 +218,7 @@ def dense_cases(only=None, pow2=False):
     need = {}
     for (M, N, K) in shapes:
         need[(N, K)] = max(need.get((N, K), 0), M)
-    big = {(N, K): I.make_normal(I.seed_for(1, 0), M, N, K, pow2=pow2) for (N, K), M in need.items()}
+    big = {(N, K): I.make_normal(I.seed_for(seed_config, 0), M, N, K, pow2=pow2) for (N, K), M in need.items()}
     cases = []
     for (M, N, K) in shapes:
         c = big[(N, K)]
@@ -247,81 +258,108 @@ def layouts_cases():
     return cases
 
 
-def contiguous_cases():
+CONTIGUOUS_SHAPES = tuple((G, base, N, K) for (N, K) in ((4096, 7168), (7168, 2048)) for G, base in ((4, 8192), (8, 4096)))
+
+
+def contiguous_cases(shapes=CONTIGUOUS_SHAPES):
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
     from oracle import oracle as O
     cases = []
-    for (N, K) in ((4096, 7168), (7168, 2048)):
-        for G, base in ((4, 8192), (8, 4096)):
-            seed = I.seed_for(2, G * 10 + base // 4096 + N)
-            sizes = I.contiguous_group_sizes(seed, G, base)
-            c = I.make_contiguous(seed, G, N, K, sizes)
-            rows = sum(sizes)
-            kb, nb = K // 128, (N + 127) // 128
-            inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb, "m_indices": c.m_indices}
-            cases.append(Case(
-                f"G{G}x{rows}rows N{N} K{K}", 2.0 * rows * N * K,
-                rows * K + G * N * K + 4 * rows * kb + 4 * G * nb * kb + 2 * rows * N + 4 * c.Mt, inp, (c.Mt, N),
-                torch.bfloat16,
-                lambda d, o, s: dg.dg_m_grouped_contiguous(d["A"], d["sfa"], d["B"], d["sfb"], d["m_indices"], o, stream=s),
-                lambda h, r: (O.m_grouped_contiguous(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], h["m_indices"][:r]),
-                              2.0 * int((h["m_indices"][:r] >= 0).sum()) * h["B"].shape[1] * h["B"].shape[2])[1]))
+    for (G, base, N, K) in shapes:
+        seed = I.seed_for(2, G * 10 + base // 4096 + N)
+        sizes = I.contiguous_group_sizes(seed, G, base)
+        c = I.make_contiguous(seed, G, N, K, sizes)
+        rows = sum(sizes)
+        kb, nb = K // 128, (N + 127) // 128
+        inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb, "m_indices": c.m_indices}
+        cases.append(Case(
+            f"G{G}x{rows}rows N{N} K{K}", 2.0 * rows * N * K,
+            rows * K + G * N * K + 4 * rows * kb + 4 * G * nb * kb + 2 * rows * N + 4 * c.Mt, inp, (c.Mt, N),
+            torch.bfloat16,
+            lambda d, o, s: dg.dg_m_grouped_contiguous(d["A"], d["sfa"], d["B"], d["sfb"], d["m_indices"], o, stream=s),
+            lambda h, r: (O.m_grouped_contiguous(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], h["m_indices"][:r]),
+                          2.0 * int((h["m_indices"][:r] >= 0).sum()) * h["B"].shape[1] * h["B"].shape[2])[1]))
     return cases
 
 
-def masked_cases():
+MASKED_SHAPES = tuple((G, max_m, em, N, K) for (N, K) in ((4096, 7168), (7168, 2048)) for G in (1, 2, 4, 16)
+                      for max_m, em in ((256, 64), (512, 128), (1024, 256)))
+
+
+def masked_sample_rows(masked_m, max_m, r):
+    """Flattened rows (g * max_m + i) of a bounded oracle sample spread over every expert: the first
+    rows of each group, up to ceil(r / G) of them, r in all at most."""
+    G = len(masked_m)
+    per = max(1, -(-r // G))
+    rows = [g * max_m + i for g in range(G) for i in range(min(per, max(0, min(int(masked_m[g]), max_m))))]
+    return rows[:r]
+
+
+def masked_cases(shapes=MASKED_SHAPES):
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
     from oracle import oracle as O
     cases = []
-    for (N, K) in ((4096, 7168), (7168, 2048)):
-        for G in (1, 2, 4, 16):
-            for max_m, em in ((256, 64), (512, 128), (1024, 256)):
-                seed = I.seed_for(3, G * 1000 + max_m + em + N)
-                sizes = I.masked_sizes(seed, G, em, max_m)
-                c = I.make_masked(seed, G, max_m, N, K, sizes, em)
-                rows = sum(sizes)
-                kb, nb = K // 128, (N + 127) // 128
-                inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb, "masked_m": c.masked_m}
-                cases.append(Case(
-                    f"G{G} max_m{max_m} E[m]{em} rows{rows} N{N} K{K}", 2.0 * rows * N * K,
-                    rows * K + G * N * K + 4 * rows * kb + 4 * G * nb * kb + 2 * rows * N, inp, (G, max_m, N),
-                    torch.bfloat16,
-                    (lambda em_: lambda d, o, s: dg.dg_m_grouped_masked(d["A"], d["sfa"], d["B"], d["sfb"], d["masked_m"], o,
-                                                                         expected_m=em_, stream=s))(em),
-                    lambda h, r: (O.m_grouped_masked(h["A"], h["sfa"], h["B"], h["sfb"], h["masked_m"],
-                                                     rows=list(range(min(r, int(h["masked_m"][0]))))),
-                                  2.0 * min(r, int(h["masked_m"][0])) * h["B"].shape[1] * h["B"].shape[2])[1]))
+    for (G, max_m, em, N, K) in shapes:
+        seed = I.seed_for(3, G * 1000 + max_m + em + N)
+        sizes = I.masked_sizes(seed, G, em, max_m)
+        c = I.make_masked(seed, G, max_m, N, K, sizes, em)
+        rows = sum(sizes)
+        kb, nb = K // 128, (N + 127) // 128
+        inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb, "masked_m": c.masked_m}
+
+        def oracle_leg(h, r, max_m=max_m):
+            sample = masked_sample_rows(h["masked_m"].tolist(), max_m, r)
+            if sample:
+                O.m_grouped_masked(h["A"], h["sfa"], h["B"], h["sfb"], h["masked_m"], rows=sample)
+            return 2.0 * len(sample) * h["B"].shape[1] * h["B"].shape[2]
+
+        cases.append(Case(
+            f"G{G} max_m{max_m} E[m]{em} rows{rows} N{N} K{K}", 2.0 * rows * N * K,
+            rows * K + G * N * K + 4 * rows * kb + 4 * G * nb * kb + 2 * rows * N, inp, (G, max_m, N),
+            torch.bfloat16,
+            (lambda em_: lambda d, o, s: dg.dg_m_grouped_masked(d["A"], d["sfa"], d["B"], d["sfb"], d["masked_m"], o,
+                                                                 expected_m=em_, stream=s))(em),
+            oracle_leg))
     return cases
 
 
-def kgrouped_cases():
+KGROUPED_SHAPES = tuple((G, M, N, 4096) for (M, N) in ((7168, 4096), (2048, 7168)) for G in (4, 8))
+
+
+def kgrouped_cases(shapes=KGROUPED_SHAPES):
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
     from oracle import oracle as O
     cases = []
-    for (M, N) in ((7168, 4096), (2048, 7168)):
-        for G in (4, 8):
-            seed = I.seed_for(4, G * 10 + M)
-            ks = I.kgrouped_sizes(seed, G, 4096)
-            c = I.make_kgrouped(seed, G, M, N, ks)
-            sumK = sum(ks)
-            inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb}
-            cases.append(Case(
-                f"G{G} M{M} N{N} sumK{sumK}", 2.0 * M * N * sumK,
-                (M + N) * sumK + 4 * (M + N) * sumK // 128 + 8 * G * M * N, inp, (G, M, N), torch.float32,
-                (lambda ks_: lambda d, o, s: dg.dg_k_grouped_wgrad(d["A"], d["sfa"], d["B"], d["sfb"], ks_, o, stream=s))(ks),
-                (lambda ks_: lambda h, r: (O.k_grouped_wgrad(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], ks_,
-                                                            np.zeros((len(ks_), min(r, h["A"].shape[0]), h["B"].shape[0]), np.float32)),
-                                           2.0 * min(r, h["A"].shape[0]) * h["B"].shape[0] * sum(ks_))[1])(ks),
-                init_out=c.D_in))
+    for (G, M, N, base_k) in shapes:
+        seed = I.seed_for(4, G * 10 + M)
+        ks = I.kgrouped_sizes(seed, G, base_k)
+        c = I.make_kgrouped(seed, G, M, N, ks)
+        sumK = sum(ks)
+        inp = {"A": c.A, "sfa": c.sfa, "B": c.B, "sfb": c.sfb}
+        cases.append(Case(
+            f"G{G} M{M} N{N} sumK{sumK}", 2.0 * M * N * sumK,
+            (M + N) * sumK + 4 * (M + N) * sumK // 128 + 8 * G * M * N, inp, (G, M, N), torch.float32,
+            (lambda ks_: lambda d, o, s: dg.dg_k_grouped_wgrad(d["A"], d["sfa"], d["B"], d["sfb"], ks_, o, stream=s))(ks),
+            (lambda ks_: lambda h, r: (O.k_grouped_wgrad(h["A"][:r], h["sfa"][:r], h["B"], h["sfb"], ks_,
+                                                        np.zeros((len(ks_), min(r, h["A"].shape[0]), h["B"].shape[0]), np.float32)),
+                                       2.0 * min(r, h["A"].shape[0]) * h["B"].shape[0] * sum(ks_))[1])(ks),
+            init_out=c.D_in))
     return cases
+
+
+def tiny_cases():
+    """The parity-sized normal GEMM, 128 x 256 x 512."""
+    return dense_cases(only=(128, 256, 512), seed_config=0)
 
 
 def build_cases(workload, shape=None, only=None):
     if workload == "dense":
         cases = dense_cases(shape)
+    elif workload == "tiny":
+        cases = tiny_cases()
     else:
         cases = {"contiguous": contiguous_cases, "masked": masked_cases, "kgrouped": kgrouped_cases,
                  "layouts": layouts_cases, "ue8m0": ue8m0_cases}[workload]()
@@ -378,23 +416,47 @@ def spin_cycles_for(host_step_s, steps):
     return int(min(2.0, 1.5 * host_step_s * (steps + 1) + 0.005) * 2.1e9)
 
 
-def run_ours(args):
+def _peaks_line(peaks):
+    """(FP8 tensor peak from the burst BF16 rate, the same from the sustained rate, HBM rate)."""
+    return 2.0 * peaks["bf16_tflops"], 2.0 * peaks["bf16_tflops_sustained"], peaks["hbm_gbs"]
+
+
+def roofline_of(workload, cases, avg_ms, peaks, peak_kind):
+    """The dominant case's roofline record and every case's fraction, against the burst FP8 peak (2 x the
+    measured burst BF16 rate) or the measured HBM rate, whichever bounds the case."""
+    fp8_peak, fp8_sustained, bw = _peaks_line(peaks)
+    per = []
+    for i, c in enumerate(cases):
+        t_tc, t_bw = c.flops / (fp8_peak * 1e12), c.bytes / (bw * 1e9)
+        per.append({"case": c.name, "ms": round(float(avg_ms[i]), 5),
+                    "tflops": round(c.flops / (avg_ms[i] * 1e-3) / 1e12, 1),
+                    "gbs": round(c.bytes / (avg_ms[i] * 1e-3) / 1e9, 1),
+                    "bound": "tensor" if t_tc >= t_bw else "hbm",
+                    "roofline_frac": round(max(t_tc, t_bw) / (avg_ms[i] * 1e-3), 3)})
+    dom = int(np.argmax(avg_ms))
+    c = cases[dom]
+    if per[dom]["bound"] == "tensor":
+        achieved, peak, unit, src = c.flops / (avg_ms[dom] * 1e-3) / 1e12, fp8_peak, "TFLOP/s", "2 x bf16_tflops (burst)"
+        sustained = round(achieved / fp8_sustained, 4)
+    else:
+        achieved, peak, unit, src = c.bytes / (avg_ms[dom] * 1e-3) / 1e9, bw, "GB/s", "hbm_gbs"
+        sustained = None
+    kernel = "dg_gemm_bs_kernel" if workload == "ue8m0" else "dg_gemm_kernel"
+    roof = {"bound": per[dom]["bound"], "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(workload, c.name),
+            "kernel": f"{kernel}, {workload} case {c.name}", "peak_source": f"{peak_kind} ({src})",
+            "frac_of_sustained": sustained, "share": round(float(avg_ms[dom] / avg_ms.sum()), 3)}
+    return roof, per
+
+
+def run_workload(workload, args, dev, world, rank, peaks, peak_kind, headline):
+    """Time one workload: the K-step timed region, the per-case and in-stream passes, e2e through host
+    buffers and the CPU oracle leg. Returns the workload's record (every rank) or None."""
     import moe_grouped_gemm_tma_gb300 as dg
     from moe_grouped_gemm_tma_gb300 import inputs as I
 
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    dg.load()
-    peaks, peak_kind = load_peaks()
-
     I.set_generation_device(dev)
-    cases = build_cases(args.workload, args.shape, args.case)
+    cases = build_cases(workload, args.shape, args.case)
     I.set_generation_device("cpu")
     # device buffers: every case its own copies (distinct addresses keep each run L2-cold)
     bufs = []
@@ -417,7 +479,7 @@ def run_ours(args):
         step()
         host_s.append(time.perf_counter() - t0)
     if dg.dg_device_status(stream) != 0:
-        raise RuntimeError("device-side timeout during warm-up")
+        raise RuntimeError(f"{workload}: device-side error during warm-up")
     host_step = min(host_s) if host_s else 0.01
 
     n = len(cases)
@@ -439,10 +501,16 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     if dg.dg_device_status(stream) != 0:
-        raise RuntimeError("device-side timeout in the timed region")
+        raise RuntimeError(f"{workload}: device-side error in the timed region")
     total_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     step_flops = sum(c.flops for c in cases)
     value = job_tflops(step_flops, args.steps, world, total_ms)
+    rec = {"value": round(value, 2), "unit": "TFLOP/s", "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(total_ms / args.steps, 4), "cases_per_step": n,
+           "gpu_launches": n * args.steps, "clocks": clk, "config": WORKLOADS[workload]
+           if args.shape is None else f"single dense GEMM M,N,K = {args.shape}"}
+    if args.timed_only:
+        return rec
 
     # per-case breakdown: a second pass with an event after every launch, also behind a spin kernel
     prof_steps = max(1, min(args.steps, 20))
@@ -481,28 +549,14 @@ def run_ours(args):
         del copies
     torch.cuda.empty_cache()
 
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    bw = peaks["hbm_gbs"]
-    per_case = []
-    for i, c in enumerate(cases):
-        t_tc, t_bw = c.flops / (fp8_peak * 1e12), c.bytes / (bw * 1e9)
-        per_case.append({"case": c.name, "ms": round(float(avg_ms[i]), 5),
-                         "tflops": round(c.flops / (avg_ms[i] * 1e-3) / 1e12, 1),
-                         "gbs": round(c.bytes / (avg_ms[i] * 1e-3) / 1e9, 1),
-                         "bound": "tensor" if t_tc >= t_bw else "hbm",
-                         "roofline_frac": round(max(t_tc, t_bw) / (avg_ms[i] * 1e-3), 3),
-                         "ms_stream": round(float(stream_ms[i]), 5),
-                         "roofline_frac_stream": round(max(t_tc, t_bw) / (stream_ms[i] * 1e-3), 3)})
-    dom = int(np.argmax(avg_ms))
-    c = cases[dom]
-    if per_case[dom]["bound"] == "tensor":
-        achieved, peak, unit, src = c.flops / (avg_ms[dom] * 1e-3) / 1e12, fp8_peak, "TFLOP/s", "2 x bf16_tflops_sustained"
-    else:
-        achieved, peak, unit, src = c.bytes / (avg_ms[dom] * 1e-3) / 1e9, bw, "GB/s", "hbm_gbs"
-    roofline = {"bound": per_case[dom]["bound"], "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload if args.shape is None else "dense", c.name),
-                "kernel": f"{'dg_gemm_bs_kernel' if args.workload == 'ue8m0' else 'dg_gemm_kernel'}, {args.workload} case {c.name}",
-                "peak_source": f"{peak_kind} ({src})", "share": round(float(avg_ms[dom] / avg_ms.sum()), 3)}
+    roof, per_case = roofline_of(workload if args.shape is None else "dense", cases, avg_ms, peaks, peak_kind)
+    fp8_peak, _, bw = _peaks_line(peaks)
+    for pc, c, ms in zip(per_case, cases, stream_ms):
+        t_bound = max(c.flops / (fp8_peak * 1e12), c.bytes / (bw * 1e9))
+        pc["ms_stream"] = round(float(ms), 5)
+        pc["roofline_frac_stream"] = round(t_bound / (ms * 1e-3), 3)
+    rec["roofline"] = roof
+    rec["per_case"] = per_case
 
     # end to end through the public API with host buffers: pinned H2D of every input, the call, D2H
     pinned, h2d, d2h = [], 0, 0
@@ -564,32 +618,65 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_value = job_tflops(step_flops, e2e_steps, world, e2e_ms)
+    rec["e2e"] = {"value": round(job_tflops(step_flops, e2e_steps, world, e2e_ms), 2), "unit": "TFLOP/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                  "pipeline": "pinned H2D, GEMM and D2H on three streams with per-case events"}
+    if dg.dg_device_status(stream) != 0:
+        raise RuntimeError(f"{workload}: device-side error in the e2e pass")
+    del pinned, bufs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     if rank == 0:
-        cpu_tf, cpu_s, cpu_fl, threads = cpu_oracle_rate(cases, CPU_SAMPLE_ROWS)
-        label = WORKLOADS[args.workload] if args.shape is None else f"single dense GEMM M,N,K = {args.shape}"
+        rows = CPU_SAMPLE_ROWS if headline else CPU_SAMPLE_ROWS_OTHER
+        cpu_tf, cpu_s, cpu_fl, threads = cpu_oracle_rate(cases, rows)
+        rec["cpu_baseline"] = {"value": cpu_tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": f"up to {rows} rows of each of the {n} cases (all rows of a smaller "
+                                         f"case; for the masked layout spread over the experts), "
+                                         f"{cpu_fl / 1e9:.1f} GFLOP in {cpu_s:.1f} s"}
+    return rec
+
+
+def run_ours(args):
+    import moe_grouped_gemm_tma_gb300 as dg
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dg.load()
+    peaks, peak_kind = load_peaks()
+
+    names = list(WORKLOAD_ORDER) if args.workload == "all" else [args.workload]
+    results = {}
+    for name in names:
+        results[name] = run_workload(name, args, dev, world, rank, peaks, peak_kind, headline=(name == names[0]))
+    head = results[names[0]]
+
+    if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-            "config": {"workload": label, "cases_per_step": n,
+            "config": {"workload": head["config"], "headline": names[0], "cases_per_step": head["cases_per_step"],
+                       "workloads_run": names,
                        "l2": "inputs larger than L2: every case has its own buffers, far above L2 per step",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "timing": "device time: CUDA events around the K steps, enqueued behind a GPU spin "
                                  "kernel so host launch cost is excluded (e2e includes it); per_case ms and "
                                  "roofline from a second pass with an event after every launch; per_case "
                                  "ms_stream from back-to-back launches of one case on distinct buffer copies"},
-            "roofline": roofline,
-            "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"first {CPU_SAMPLE_ROWS} rows (all rows of a smaller case) of each of the {n} cases "
-                                       f"({cpu_fl / 1e9:.1f} GFLOP in {cpu_s:.1f} s)"},
-            "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "pipeline": "pinned H2D, GEMM and D2H on three streams with per-case events"},
-            "clocks": clk,
-            "gpu_launches": n * args.steps,
-            "per_case": per_case,
+            "roofline": head.get("roofline"),
+            "cpu_baseline": head.get("cpu_baseline"),
+            "e2e": head.get("e2e"),
+            "clocks": head["clocks"],
+            "gpu_launches": head["gpu_launches"],
+            "per_case": head.get("per_case"),
+            "per_workload": {k: v for k, v in results.items() if k != names[0]},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -603,7 +690,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
+    ap.add_argument("--workload", choices=["all"] + sorted(WORKLOADS), default="all",
+                    help="one workload, or all of them (the default; the dense workload is the headline)")
+    ap.add_argument("--timed-only", action="store_true",
+                    help="run the warm-up and timed steps alone (no per-case, e2e or CPU passes): for profiler captures")
     ap.add_argument("--shape", default=None,
                     help="M,N,K: time only this GEMM of the dense workload (for profiler captures)")
     ap.add_argument("--case", default=None,
@@ -613,6 +703,8 @@ def main():
         args.shape = tuple(int(x) for x in args.shape.split(","))
         args.workload = "dense"
     if args.impl == "reference":
+        if args.workload == "all":
+            args.workload = HEADLINE
         return run_reference(args)
     return run_ours(args)
 

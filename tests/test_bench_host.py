@@ -128,3 +128,39 @@ def test_cpu_baseline_counts_each_cases_own_flops(workload, monkeypatch):
         for r in (16, 100, 5000):
             assert c.oracle(host, r) == 2.0 * min(r, M) * N * K, (c.name, r)
         assert c.flops == 2.0 * M * N * K
+
+
+def test_cpu_baseline_counts_grouped_layouts_flops():
+    # the grouped workloads' oracle legs, on small shapes built by the same case builders: each reports
+    # 2 * (rows it computed) * N * K, and the masked leg samples every expert, not only the first
+    import numpy as np
+    for c in bench.contiguous_cases(shapes=((2, 256, 256, 256),)):
+        host = dict(c.inputs)
+        N, K = c.inputs["B"].shape[1], c.inputs["B"].shape[2]
+        for r in (16, 300, 10 ** 6):
+            valid = int((c.inputs["m_indices"][:r] >= 0).sum())
+            assert c.oracle(host, r) == 2.0 * valid * N * K
+    for c in bench.masked_cases(shapes=((3, 64, 32, 256, 256),)):
+        mm = c.inputs["masked_m"].tolist()
+        assert len(mm) == 3 and all(m > 0 for m in mm)
+        rows = bench.masked_sample_rows(mm, 64, 6)
+        assert sorted({r // 64 for r in rows}) == [0, 1, 2]          # every expert is sampled
+        assert all(r % 64 < mm[r // 64] for r in rows)               # only valid rows
+        host = dict(c.inputs)
+        assert c.oracle(host, 6) == 2.0 * len(rows) * 256 * 256
+        assert c.oracle(host, 10 ** 6) == 2.0 * sum(mm) * 256 * 256
+        assert c.flops == 2.0 * sum(mm) * 256 * 256
+    for c in bench.kgrouped_cases(shapes=((2, 128, 128, 256),)):
+        sumK = c.inputs["A"].shape[1]
+        host = dict(c.inputs)
+        for r in (16, 1000):
+            assert c.oracle(host, r) == 2.0 * min(r, 128) * 128 * sumK
+    assert bench.masked_sample_rows([0, 5, 0], 8, 4) == [8, 9]                  # ceil(4 / 3) rows a group
+    assert bench.masked_sample_rows([100, 100], 64, 3) == [0, 1, 64]
+
+
+def test_default_run_covers_every_workload():
+    assert set(bench.WORKLOAD_ORDER) == set(bench.WORKLOADS)
+    assert bench.WORKLOAD_ORDER[0] == bench.HEADLINE == "dense"
+    for w in ("contiguous", "masked", "kgrouped", "tiny"):
+        assert w in bench.WORKLOAD_ORDER
