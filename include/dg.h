@@ -25,7 +25,7 @@
  *   - The library runs on compute capability 10.3 only (sm_103a code); other devices get
  *     DG_NO_DEVICE_SUPPORT.
  *   - Device-side waits are bounded; a kernel that gives up records DG_DEVICE_TIMEOUT, which
- *     dg_device_status() reports.
+ *     dg_device_status() reports. Tuning overrides and a test hook for this path: dg_tuning.h.
  *   - Distinct streams may call concurrently (no mutable host state after first use per device).
  */
 #ifndef DG_H
@@ -155,9 +155,12 @@ dg_status dg_wgrad_fp8_nt(const uint8_t* A, const float* sfa, const uint8_t* B, 
 const char* dg_status_string(dg_status status);
 
 /*
- * Synchronises `stream`, then reports (and clears) a device-side timeout recorded by any dg kernel
- * on the current device since the last call: DG_DEVICE_TIMEOUT, or DG_SCALE_NOT_UE8M0 from the UE8M0
- * path, else DG_CUDA_ERROR if the synchronisation failed, else DG_OK.
+ * Synchronises `stream`, then reports (and clears) the device-side error recorded by any dg kernel on
+ * the current device since the last call: DG_DEVICE_TIMEOUT, or DG_SCALE_NOT_UE8M0 from the UE8M0
+ * path, else DG_CUDA_ERROR if the synchronisation failed, else DG_OK. Kernels record only the first
+ * error (a later one does not overwrite it). Reading and clearing are two steps: an error that a dg
+ * kernel on another stream records between them is lost, so call this while no other dg work runs on
+ * the device when every error must be seen.
  */
 dg_status dg_device_status(cudaStream_t stream);
 

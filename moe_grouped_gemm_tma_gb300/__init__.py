@@ -12,6 +12,7 @@ layouts and the k-grouped FP32 weight gradient.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -20,6 +21,7 @@ __all__ = [
     "DGError", "load", "dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_gemm_fp8_nt_ue8m0_packed",
     "dg_m_grouped_contiguous", "dg_m_grouped_masked",
     "dg_k_grouped_wgrad", "dg_wgrad_fp8_nt", "dg_device_status", "dg_status_string", "scale_shapes", "library_path",
+    "TUNE_KNOBS", "dg_tuning_set", "dg_tuning_get", "dg_tuning_reset", "tuning", "dg_testing_arm_wait_timeout",
 ]
 
 _lock = threading.Lock()
@@ -61,6 +63,14 @@ def load(build_if_missing: bool = True):
             L.dg_k_grouped_wgrad.argtypes = [P, P, P, P, P, P, I, I, I, P]
             L.dg_wgrad_fp8_nt.argtypes = [P, P, P, P, P, I, I, I, I, P]
             L.dg_device_status.argtypes = [P]
+            L.dg_tuning_set.argtypes = [I, I]
+            L.dg_tuning_set.restype = I
+            L.dg_tuning_get.argtypes = [I]
+            L.dg_tuning_get.restype = I
+            L.dg_tuning_reset.argtypes = []
+            L.dg_tuning_reset.restype = None
+            L.dg_testing_arm_wait_timeout.argtypes = [ctypes.c_uint64]
+            L.dg_testing_arm_wait_timeout.restype = I
             L.dg_status_string.argtypes = [I]
             L.dg_status_string.restype = ctypes.c_char_p
             for f in ("dg_gemm_fp8_nt", "dg_gemm_fp8", "dg_gemm_fp8_nt_ue8m0", "dg_gemm_fp8_nt_ue8m0_packed",
@@ -287,3 +297,39 @@ def dg_device_status(stream=None) -> int:
 
 def dg_status_string(status: int) -> str:
     return load().dg_status_string(int(status)).decode()
+
+
+# Tuning knobs (include/dg_tuning.h): overrides of the automatic tile-shape choice, for sweeps and for
+# tests that must reach one kernel specialisation. -1 (or None) is the automatic choice.
+TUNE_KNOBS = {"bn": 0, "pair": 1, "split": 2, "swap": 3, "group_m": 4, "pdl": 5}
+
+
+def dg_tuning_set(knob, value) -> None:
+    k = TUNE_KNOBS[knob] if isinstance(knob, str) else int(knob)
+    _check(load().dg_tuning_set(k, -1 if value is None else int(value)), "dg_tuning_set")
+
+
+def dg_tuning_get(knob) -> int:
+    return load().dg_tuning_get(TUNE_KNOBS[knob] if isinstance(knob, str) else int(knob))
+
+
+def dg_tuning_reset() -> None:
+    load().dg_tuning_reset()
+
+
+@contextlib.contextmanager
+def tuning(**knobs):
+    """Set tuning knobs (bn=, pair=, split=, swap=, group_m=, pdl=) for the duration of a ``with`` block;
+    every knob returns to the automatic choice afterwards."""
+    try:
+        for k, v in knobs.items():
+            dg_tuning_set(k, v)
+        yield
+    finally:
+        dg_tuning_reset()
+
+
+def dg_testing_arm_wait_timeout(wait_limit_ns: int) -> None:
+    """Test hook: the next launch of the main kernel bounds its waits by ``wait_limit_ns`` and leaves its
+    first pipeline stage unfilled, so that a wait runs out and the kernel reports DG_DEVICE_TIMEOUT."""
+    _check(load().dg_testing_arm_wait_timeout(int(wait_limit_ns)), "dg_testing_arm_wait_timeout")

@@ -1,6 +1,8 @@
-"""Build ``_build/libdg.so`` from ``csrc/`` with nvcc for sm_103a (parallel translation units)."""
+"""Build ``_build/libdg.so`` from ``csrc/`` with nvcc for sm_103a (parallel translation units); rebuilt
+whenever the digest of its sources differs from the one recorded beside it."""
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -14,7 +16,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdg.so")
 
 SOURCES = ["dg_api.cu", "dg_inst_normal.cu", "dg_inst_contiguous.cu", "dg_inst_masked.cu", "dg_inst_kgrouped.cu",
-           "dg_inst_bs.cu", "dg_inst_swap.cu"]
+           "dg_inst_bs.cu", "dg_inst_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -25,18 +27,41 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libdg")
 
 
-def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "dg.h"), __file__]
-    return max(os.path.getmtime(f) for f in files)
+STAMP = LIB + ".sha256"
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
+
+
+def source_digest() -> str:
+    """SHA-256 over every input of the build: the CUDA sources and headers, the public headers, this
+    script and the compiler flags. The library is rebuilt whenever it differs from the digest recorded
+    beside it (file times are not trusted: a copied tree can carry a library newer than its sources)."""
+    h = hashlib.sha256()
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+    files += sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
+    files.append(os.path.abspath(__file__))
+    for f in files:
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(FLAGS + SOURCES).encode())
+    return h.hexdigest()
+
+
+def up_to_date() -> bool:
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
+        return False
+    with open(STAMP) as f:
+        return f.read().strip() == source_digest()
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every translation unit in parallel and link the shared library; returns its path."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
+    if not force and up_to_date():
         return LIB
+    digest = source_digest()
     cc = nvcc()
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    flags = FLAGS + ["-I", INCLUDE, "-I", CSRC]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
     procs, objs = [], []
@@ -58,6 +83,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     link = [cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "--no-undefined", *objs, "-o", tmp]
     subprocess.run(link, check=True)
     os.replace(tmp, LIB)
+    with open(STAMP + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(STAMP + f".tmp{os.getpid()}", STAMP)
     return LIB
 
 

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -15,10 +16,40 @@
 
 #include "dg.h"
 #include "dg_launch.cuh"
+#include "dg_tuning.h"
 
 namespace dg {
 
 __device__ int g_status_word;
+
+namespace {
+
+// Tuning knobs (dg_tuning.h) and the armed test fault. The environment is read once, at load, and only
+// when DG_TUNING=1.
+std::atomic<int> g_tune[DG_TUNE_COUNT];
+std::atomic<unsigned long long> g_armed_wait_fault{0};
+
+struct TuneInit {
+    TuneInit() {
+        for (auto& k : g_tune) k.store(DG_TUNE_AUTO);
+        const char* on = getenv("DG_TUNING");
+        if (!on || strcmp(on, "1") != 0) return;
+        const char* names[DG_TUNE_COUNT] = {"DG_BN", "DG_PAIR", "DG_SPLIT", "DG_SWAP", "DG_GROUP_M", "DG_PDL"};
+        for (int i = 0; i < DG_TUNE_COUNT; ++i)
+            if (const char* v = getenv(names[i])) g_tune[i].store(atoi(v));
+    }
+} g_tune_init;
+
+}  // namespace
+
+int tune(int knob) {
+    return (knob >= 0 && knob < DG_TUNE_COUNT) ? g_tune[knob].load(std::memory_order_relaxed) : DG_TUNE_AUTO;
+}
+
+unsigned long long take_armed_wait_fault() {
+    if (g_armed_wait_fault.load(std::memory_order_relaxed) == 0) return 0;
+    return g_armed_wait_fault.exchange(0);
+}
 
 namespace {
 
@@ -182,12 +213,11 @@ Spec choose_spec(const Spec (&cands)[NC], int64_t row_units, int n, int sms) {
     return best;
 }
 
-// Optional override of the tile width, for tuning sweeps only (DG_BN=<n>); ignored unless valid.
+// Optional override of the tile width (the DG_TUNE_BN knob); ignored unless the layout has that width.
 template <size_t NC>
 Spec spec_override(const Spec (&cands)[NC], Spec chosen) {
-    const char* s = getenv("DG_BN");
-    if (!s) return chosen;
-    const int v = atoi(s);
+    const int v = tune(DG_TUNE_BN);
+    if (v < 0) return chosen;
     for (size_t i = 0; i < NC; ++i)
         if (cands[i].bn == v) return cands[i];
     return chosen;
@@ -198,7 +228,7 @@ Spec spec_override(const Spec (&cands)[NC], Spec chosen) {
 // while the band sweeps every column block; with the plain row-fastest order a wave spans up to 152 row
 // blocks of one column block, and once A outgrows L2 every column block re-reads A from DRAM (measured
 // on the contiguous layout with 31k rows, K = 7168: 803 us row-fastest, 691 us in bands of 16).
-// DG_GROUP_M=<n> forces the band height for sweeps.
+// The DG_TUNE_GROUP_M knob forces the band height.
 int choose_group_m(int m_blocks, int tile_m, int64_t k, const DeviceInfo& dev) {
     int gm = std::min(m_blocks, 16);
     const int64_t band_bytes = static_cast<int64_t>(tile_m) * k;
@@ -206,10 +236,7 @@ int choose_group_m(int m_blocks, int tile_m, int64_t k, const DeviceInfo& dev) {
         const int64_t fit = (static_cast<int64_t>(dev.l2_bytes) / 3) / band_bytes;
         gm = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(fit, gm)));
     }
-    if (const char* e = getenv("DG_GROUP_M")) {
-        const int v = atoi(e);
-        if (v > 0) gm = std::min(v, m_blocks);
-    }
+    if (const int v = tune(DG_TUNE_GROUP_M); v > 0) gm = std::min(v, m_blocks);
     return std::max(gm, 1);
 }
 
@@ -218,15 +245,11 @@ int choose_group_m(int m_blocks, int tile_m, int64_t k, const DeviceInfo& dev) {
 // the most CTAs that still fit in one wave, at least `min_kb` K blocks per CTA (4; the block-scaled
 // kernel, whose per-CTA set-up is longer, asks for 8: 64 x 7168 x 2048 took 22.7 us as 4 CTAs of 4
 // blocks per tile, against 14.4 us unsplit); ties go to the smaller S.
-// DG_SPLIT=<s> forces S (2, 4 or 8; 1 disables) for sweeps.
+// The DG_TUNE_SPLIT knob forces S (2, 4 or 8; 1 disables); a forced tile width disables the split.
 template <size_t NC>
 int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, int kbs, int sms, int min_kb = 4) {
-    const char* env = getenv("DG_SPLIT");
-    if (env) {
-        const int s = atoi(env);
-        return (s == 2 || s == 4 || s == 8) && kbs >= s ? s : 1;
-    }
-    if (getenv("DG_BN")) return 1;
+    if (const int s = tune(DG_TUNE_SPLIT); s >= 0) return (s == 2 || s == 4 || s == 8) && kbs >= s ? s : 1;
+    if (tune(DG_TUNE_BN) >= 0) return 1;
     if (row_blocks * cdiv(n, sp->bn) * 2 > sms) return 1;
     int best_split = 1;
     int64_t best_ctas = row_blocks * cdiv(n, sp->bn);
@@ -246,11 +269,9 @@ int choose_split(const Spec (&cands)[NC], Spec* sp, int64_t row_blocks, int n, i
 
 // CTA-pair (256-row) tiles halve the per-SM B traffic, but with the promotion epilogue as the limit
 // they currently lose to single-CTA tiles on every measured shape (the cross-SM accumulator handoff
-// lengthens the MMA/promotion loop), so they are opt-in: DG_PAIR=2 (only for more than 128 rows).
-bool use_pair(int64_t rows_per_group) {
-    const char* s = getenv("DG_PAIR");
-    return s && atoi(s) == 2 && rows_per_group > 128;
-}
+// lengthens the MMA/promotion loop), so they are opt-in: the DG_TUNE_PAIR knob at 2 (only for more
+// than 128 rows).
+bool use_pair(int64_t rows_per_group) { return tune(DG_TUNE_PAIR) == 2 && rows_per_group > 128; }
 
 template <int MODE>
 cudaError_t launch_spec(Spec sp, const Launch& L);
@@ -288,6 +309,60 @@ cudaError_t launch_spec<kKGrouped>(Spec sp, const Launch& L) {
     return cudaErrorInvalidValue;
 }
 #undef DG_CASE
+
+// The few-row (decode) kernel's plan: tile height BMT (tokens per tile, the MMA's N) from the expected
+// rows per expert, and the split-K cluster size S. Time per wave of clusters ~ K blocks per CTA plus a
+// fixed per-tile cost (the reduction through distributed shared memory for S > 1), so S is the one that
+// minimises waves x (K/S + overhead) over the clusters that can be resident at once; ties go to the
+// smaller S. The DG_TUNE_SPLIT knob forces S (1, 2, 4 or 8, at most the K blocks).
+struct DecodePlan {
+    int bmt = 64;
+    int split = 1;
+    int units = 0;   // clusters (or CTAs) launched: persistent, at most one wave
+};
+
+template <int MODE>
+int decode_capacity(int bmt, int split, int sms) {
+    switch (bmt) {
+        case 32: return decode_cluster_capacity<MODE, 32>(split, sms);
+        case 64: return decode_cluster_capacity<MODE, 64>(split, sms);
+        default: return decode_cluster_capacity<MODE, 128>(split, sms);
+    }
+}
+
+template <int MODE>
+DecodePlan plan_decode(int64_t groups, int rows_hint, int rows_max, int n, int kbs, int sms) {
+    DecodePlan pl;
+    pl.bmt = rows_hint <= 32 ? 32 : (rows_hint <= 64 ? 64 : 128);
+    const int64_t nt = cdiv(n, 128);
+    const int64_t tiles_exp = std::max<int64_t>(1, groups * cdiv(std::max(rows_hint, 1), pl.bmt) * nt);
+    const int64_t tiles_max = groups * cdiv(std::max(rows_max, 1), pl.bmt) * nt;
+    const int forced = tune(DG_TUNE_SPLIT);
+    const bool force = (forced == 1 || forced == 2 || forced == 4 || forced == 8) && kbs >= forced;
+    int64_t best = INT64_MAX;
+    for (int s = 1; s <= 8; s *= 2) {
+        if (force ? s != forced : (s > 1 && kbs < 2 * s)) continue;
+        const int cap = std::max(1, decode_capacity<MODE>(pl.bmt, s, sms));
+        const int64_t waves = (tiles_exp + cap - 1) / cap;
+        const int64_t cost = waves * (cdiv(kbs, s) + (s > 1 ? 3 : 1));
+        if (cost < best) {
+            best = cost;
+            pl.split = s;
+            pl.units = static_cast<int>(std::min<int64_t>(tiles_max, cap));
+        }
+    }
+    return pl;
+}
+
+template <int MODE>
+cudaError_t launch_decode_bmt(int bmt, const Launch& L) {
+    switch (bmt) {
+        case 32: return launch_decode<MODE, 32>(L);
+        case 64: return launch_decode<MODE, 64>(L);
+        case 128: return launch_decode<MODE, 128>(L);
+    }
+    return cudaErrorInvalidValue;
+}
 
 dg_status common_prologue(DeviceInfo* dev) {
     dg_status st = device_info(dev);
@@ -397,54 +472,39 @@ static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B,
     Launch L;
     std::memset(&L, 0, sizeof(L));
     const int kbs = K / 128;
-    if (!a_mn && !b_mn && !pair && M <= 128) {
-        // Few rows: the swapped-operand kernel stages 128 B rows plus M A rows per K block instead of
-        // 128 A rows plus BN B rows. Take it when it moves fewer operand bytes per CTA (waves x K blocks
-        // per CTA x bytes per K block) and each CTA streams a long K (its per-tile exchange, column
-        // stores and reduction cost more than they save below ~32 K blocks: measured 64 x 7168 x 16384
-        // 47.7 -> 37.5 us, while 128 x 7168 x 2048 went 15 -> 19 us); DG_SWAP=0 / 1 forces the choice.
-        const int bmt = M <= 32 ? 32 : (M <= 64 ? 64 : 128);
-        const int nt = cdiv(N, 128);
-        int s_sw = 1;
-        for (int s = 2; s <= 4; s *= 2)
-            if (kbs >= 4 * s && static_cast<int64_t>(nt) * s <= dev.sms) s_sw = s;
-        const int64_t cost_sw = cdiv(static_cast<int64_t>(nt) * s_sw, dev.sms) * cdiv(kbs, s_sw) *
-                                static_cast<int64_t>(bmt * 128 + 128 * 128);
-        const int64_t tiles_std = static_cast<int64_t>(cdiv(M, BM)) * cdiv(N, bn);
-        const int64_t cost_std = cdiv(tiles_std * split, dev.sms) * cdiv(kbs, split) *
-                                 static_cast<int64_t>(128 * 128 + bn * 128);
-        bool swap = cost_sw < cost_std && cdiv(kbs, s_sw) >= 32;
-        if (const char* e = getenv("DG_SWAP")) swap = (e[0] == '1');
-        if (swap) {
-            if (make_operand_map(&L.tmap_a, A, M, K, bmt) != DG_OK) return DG_CUDA_ERROR;
-            if (make_operand_map(&L.tmap_b, B, N, K, 128) != DG_OK) return DG_CUDA_ERROR;
-            if (make_output_map(&L.tmap_d, D, M, N) != DG_OK) return DG_CUDA_ERROR;
-            Params& p = L.params;
-            p.sfa = sfa;
-            p.sfb = sfb;
-            p.d = D;
-            p.status = dev.status;
-            p.rows = M;
-            p.n = N;
-            p.kbs = kbs;
-            p.groups = 1;
-            p.sfb_rows = cdiv(N, 128);
-            p.m_blocks = cdiv(M, bmt);
-            p.n_blocks = nt;
-            p.group_m = 1;
-            p.split = s_sw;
-            p.tiles = p.m_blocks * p.n_blocks;
-            L.units = p.tiles;
-            L.sms = dev.sms;
-            L.stream = stream;
-            cudaError_t e = cudaErrorInvalidValue;
-            switch (bmt) {
-                case 32: e = launch_swap<32>(L); break;
-                case 64: e = launch_swap<64>(L); break;
-                case 128: e = launch_swap<128>(L); break;
-            }
-            return e == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
-        }
+    // Few rows with a long K per CTA: the decode kernel (swapped operands, K-block groups, split-K
+    // clusters sized to fill the SMs). With short K per CTA its per-tile set-up and reduction cost more
+    // than its fuller stages save, and the standard kernel with split-K is faster (measured: 64 x 7168 x
+    // 16384 35.0 against 43.7 us; 64 x 2112 x 7168 18.6 against 14.5 us). The DG_TUNE_SWAP knob forces
+    // the choice (1 = decode kernel, 0 = standard kernel).
+    DecodePlan pl;
+    bool decode = false;
+    if (!a_mn && !b_mn && !pair && M <= 128 && tune(DG_TUNE_BN) < 0) {
+        pl = plan_decode<kNormal>(1, M, M, N, kbs, dev.sms);
+        decode = cdiv(kbs, pl.split) >= 32;
+        if (const int v = tune(DG_TUNE_SWAP); v >= 0) decode = (v == 1);
+    }
+    if (decode) {
+        if (make_operand_map(&L.tmap_a, A, M, K, pl.bmt) != DG_OK) return DG_CUDA_ERROR;
+        if (make_operand_map(&L.tmap_b, B, N, K, 128) != DG_OK) return DG_CUDA_ERROR;
+        Params& p = L.params;
+        p.sfa = sfa;
+        p.sfb = sfb;
+        p.d = D;
+        p.status = dev.status;
+        p.rows = M;
+        p.n = N;
+        p.kbs = kbs;
+        p.groups = 1;
+        p.sfb_rows = cdiv(N, 128);
+        p.m_blocks = cdiv(M, pl.bmt);
+        p.n_blocks = cdiv(N, 128);
+        p.split = pl.split;
+        p.tiles = p.m_blocks * p.n_blocks;
+        L.units = pl.units;
+        L.sms = dev.sms;
+        L.stream = stream;
+        return launch_decode_bmt<kNormal>(pl.bmt, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
     }
     if ((a_mn ? make_mn_operand_map(&L.tmap_a, A, K, M) : make_operand_map(&L.tmap_a, A, M, K, BM)) != DG_OK)
         return DG_CUDA_ERROR;
@@ -492,6 +552,24 @@ const char* dg_status_string(dg_status s) {
     return "DG_UNKNOWN_STATUS";
 }
 
+dg_status dg_tuning_set(int knob, int value) {
+    if (knob < 0 || knob >= DG_TUNE_COUNT) return DG_INVALID_ARG;
+    g_tune[knob].store(value < 0 ? DG_TUNE_AUTO : value);
+    return DG_OK;
+}
+
+int dg_tuning_get(int knob) { return tune(knob); }
+
+void dg_tuning_reset(void) {
+    for (auto& k : g_tune) k.store(DG_TUNE_AUTO);
+}
+
+dg_status dg_testing_arm_wait_timeout(uint64_t wait_limit_ns) {
+    if (wait_limit_ns == 0) return DG_INVALID_ARG;
+    g_armed_wait_fault.store(static_cast<unsigned long long>(wait_limit_ns));
+    return DG_OK;
+}
+
 dg_status dg_device_status(cudaStream_t stream) {
     DeviceInfo dev;
     dg_status st = device_info(&dev);
@@ -537,9 +615,9 @@ static dg_status ue8m0_impl(const uint8_t* A, const void* sfa, const uint8_t* B,
     // CTA pairs halve each SM's B bytes per K block, which the block-scaled kernel (no per-block
     // promotion loop) turns into speed: 4096 x 7168 x 16384 in 279 us against 308 us single-CTA, and
     // faster on every M = 4096 dense shape. They are taken when the pair tiles fill at least one wave
-    // of CTAs; fewer tiles go to single-CTA tiles with split-K. DG_PAIR=1 / 2 forces the choice.
+    // of CTAs; fewer tiles go to single-CTA tiles with split-K. The DG_TUNE_PAIR knob forces the choice.
     bool pair = M > BM && static_cast<int64_t>(cdiv(M, 2 * BM)) * cdiv(N, 256) * 2 >= dev.sms;
-    if (const char* e = getenv("DG_PAIR")) pair = (atoi(e) == 2) && M > BM;
+    if (const int v = tune(DG_TUNE_PAIR); v >= 0) pair = (v == 2) && M > BM;
     Spec sp = pair ? spec_override(kBlockScaledSpecs2, choose_spec(kBlockScaledSpecs2, cdiv(M, 2 * BM), N, dev.sms))
                    : spec_override(kBlockScaledSpecs, choose_spec(kBlockScaledSpecs, cdiv(M, BM), N, dev.sms));
     const int split = pair ? 1 : choose_split(kBlockScaledSpecs, &sp, cdiv(M, BM), N, K / 128, dev.sms, 8);
@@ -662,6 +740,36 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     if (st != DG_OK) return st;
 
     const int hint = (expected_m > 0 && expected_m < max_m) ? expected_m : max_m;
+    if (hint <= 128 && tune(DG_TUNE_SWAP) == 1 && tune(DG_TUNE_PAIR) != 2 && tune(DG_TUNE_BN) < 0) {
+        // Decode: few rows per expert. The decode kernel (swapped operands: B's rows fill the MMA's 128
+        // lanes, the tokens are its N) counts each expert's row blocks on the device from masked_m; the
+        // plan (tile height, split-K) follows expected_m, and any masked_m up to max_m stays correct.
+        const DecodePlan pl = plan_decode<kMasked>(G, hint, max_m, N, K / 128, dev.sms);
+        Launch L;
+        std::memset(&L, 0, sizeof(L));
+        if (make_operand_map(&L.tmap_a, A, static_cast<int64_t>(G) * max_m, K, pl.bmt) != DG_OK) return DG_CUDA_ERROR;
+        if (make_operand_map(&L.tmap_b, B, static_cast<int64_t>(G) * N, K, 128) != DG_OK) return DG_CUDA_ERROR;
+        Params& p = L.params;
+        p.sfa = sfa;
+        p.sfb = sfb;
+        p.d = D;
+        p.masked_m = masked_m;
+        p.status = dev.status;
+        p.rows = max_m;
+        p.n = N;
+        p.kbs = K / 128;
+        p.groups = G;
+        p.sfb_rows = cdiv(N, 128);
+        p.m_blocks = cdiv(max_m, pl.bmt);
+        p.n_blocks = cdiv(N, 128);
+        if (static_cast<int64_t>(G) * p.m_blocks * p.n_blocks > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
+        p.tiles = 0;  // counted on the device from masked_m
+        p.split = pl.split;
+        L.units = pl.units;
+        L.sms = dev.sms;
+        L.stream = stream;
+        return launch_decode_bmt<kMasked>(pl.bmt, L) == cudaSuccess ? DG_OK : DG_CUDA_ERROR;
+    }
     const bool pair = use_pair(hint);
     Spec sp = pair ? spec_override(kMaskedSpecs2, choose_spec(kMaskedSpecs2, static_cast<int64_t>(G) * cdiv(hint, 2 * BM), N, dev.sms))
                    : spec_override(kMaskedSpecs1, choose_spec(kMaskedSpecs1, static_cast<int64_t>(G) * cdiv(hint, BM), N, dev.sms));

@@ -41,9 +41,10 @@
 // Barrier round trips cost about a hundred cycles each, so the loops probe all barriers of a pass at
 // once, and on narrow tiles the producer, MMA issuer and stager take a second ready K block per pass.
 //
-// Every wait is bounded: after WAIT_LIMIT_NS a waiter records DG_DEVICE_TIMEOUT in the status word,
-// raises a CTA-wide abort flag, and the CTA drains its own in-flight copies and MMAs (bounded too),
-// frees TMEM and exits.
+// Every wait is bounded: after the launch's wait limit (WAIT_LIMIT_NS unless a test shortens it) a
+// waiter records DG_DEVICE_TIMEOUT in the status word (the first error recorded wins), raises a
+// CTA-wide abort flag, and the CTA drains its own in-flight copies and MMAs (bounded too), frees TMEM
+// and exits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -93,6 +94,9 @@ struct Params {
     int a_mn, b_mn;            // normal layout: A stored [K, M] / B stored [K, N] (MN-major operands)
     int sf_packed;             // block-scaled: sfa / sfb hold UE8M0 exponents, four K blocks per int32
     int sf_words;              // block-scaled, packed: int32 words per scale row, ceil(kbs / 4)
+    unsigned long long wait_limit_ns;  // bound of every wait (0 = WAIT_LIMIT_NS); tests shorten it
+    int fault_skip_first_fill;  // test only (0 in every product call): the producer leaves its first
+                                // stage unfilled, so the MMA issuer's wait on it runs out
     int kb_off[MAX_KGROUPS + 1];  // k-grouped: first K block of each expert, kb_off[G] = sumK/128
 };
 
@@ -266,20 +270,26 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
     return ti;
 }
 
+// Record a device-side error in the status word unless one is recorded already (the first error since
+// the host last read and cleared the word wins; a later one does not overwrite it).
+__device__ __forceinline__ void record_status(int* status, int code) { atomicCAS(status, 0, code); }
+
 // Bounded mbarrier wait. Returns false when this CTA is aborting (this waiter timed out, or another
-// role did); the first waiter to time out records the status and raises the abort flag.
+// role did); the first waiter to time out records the status and raises the abort flag. `limit_ns` is
+// the launch's wait limit (0 = WAIT_LIMIT_NS).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             int* status) {
+                                             int* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit = limit_ns ? limit_ns : WAIT_LIMIT_NS;
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit) {
             *abort_flag = 1;
-            atomicExch(status, STATUS_TIMEOUT);
+            record_status(status, STATUS_TIMEOUT);
             return false;
         }
     }
@@ -455,6 +465,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;   // per-stage bits, for the abort drain
             bool ok = true;
+            bool skip_fill = p.fault_skip_first_fill != 0;   // test only: leave the first stage empty
             for (int t = unit; t < num_tiles && ok; t += num_units) {
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
@@ -469,13 +480,20 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
                     const bool f0 = mbar_try_wait(&empty_bar[stage], phase ^ 1u);
                     const bool f1 = more && mbar_test_wait(&empty_bar[s1], ph1 ^ 1u);
-                    const bool got = f0 || wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                    const bool got = f0 || wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
                     for (int j = 0; j < take; ++j) {
                         const int x = (ti.kb0 + kb + j) * BK;
                         uint8_t* a_dst = smem_a + stage * C::A_BYTES;
                         uint8_t* b_dst = smem_b + stage * C::B_BYTES;
+                        if (skip_fill) {
+                            // test only: no expect_tx, no copy, so this stage's `full` phase never
+                            // completes and the MMA issuer's bounded wait on it expires
+                            skip_fill = false;
+                            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                            continue;
+                        }
                         if (PAIR == 1 || leader) {
                             if (issuer) {
                                 mbar_arrive_expect_tx(&full_bar[stage], PAIR * C::STAGE_BYTES);
@@ -509,7 +527,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 // wait until every stage this CTA filled has been consumed, so no MMA-completion
                 // arrival can still be in flight towards this CTA when it exits
                 for (int i = 0; i < STAGES && ok; ++i) {
-                    const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                    const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) ok = false;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -547,8 +565,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                                              static_cast<unsigned>(mbar_test_wait(&full_bar[s1], ph1))) != 0u;
                     bool got = r0;
                     if (!got)
-                        got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status) &&
-                              wait_bounded(&full_bar[stage], phase, abort_flag, p.status);
+                        got = wait_bounded(&tmem_empty_bar[acc], acc_phase ^ 1u, abort_flag, p.status, p.wait_limit_ns) &&
+                              wait_bounded(&full_bar[stage], phase, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const int take = __all_sync(0xffffffffu, r1) ? 2 : 1;
                     tc_fence_after();
@@ -617,7 +635,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
                     const bool f0 = mbar_try_wait(&scale_empty_bar[slot], sphase ^ 1u);
                     const bool f1 = more && mbar_test_wait(&scale_empty_bar[s1], sp1 ^ 1u);
-                    const bool got = f0 || wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                    const bool got = f0 || wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
                     for (int j = 0; j < take; ++j) {
@@ -676,8 +694,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_full_bar[acc], acc_phase)) &
                                 static_cast<unsigned>(mbar_try_wait(&scale_full_bar[slot], sphase))) != 0u;
                     if (!got)
-                        got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
-                              wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
+                        got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status, p.wait_limit_ns) &&
+                              wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t taddr = lane_addr + static_cast<uint32_t>(acc * BN);
@@ -753,8 +771,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_full_bar[acc], acc_phase)) &
                                     static_cast<unsigned>(mbar_try_wait(&scale_full_bar[slot], sphase))) != 0u;
                         if (!got)
-                            got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status) &&
-                                  wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status);
+                            got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status, p.wait_limit_ns) &&
+                                  wait_bounded(&scale_full_bar[slot], sphase, abort_flag, p.status, p.wait_limit_ns);
                         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                         tc_fence_after();
                         // TMEM loads in batches of up to 64 columns (the registers next to BN running
@@ -808,7 +826,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const float4* theirs = reinterpret_cast<const float4*>(s_xchg) + ((1 - h) * BM + row_in_tile) * HC;
 #pragma unroll
                 for (int ps = 0; ps < COLS / PASS; ++ps) {
-                    const bool freed = wait_bounded(&xchg_free_bar, xphase ^ 1u, abort_flag, p.status);
+                    const bool freed = wait_bounded(&xchg_free_bar, xphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, freed)) { ok = false; break; }
 #pragma unroll
                     for (int c = 0; c < HC; ++c) {
@@ -817,7 +835,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&xchg_full_bar);
-                    const bool full = wait_bounded(&xchg_full_bar, xphase, abort_flag, p.status);
+                    const bool full = wait_bounded(&xchg_full_bar, xphase, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, full)) { ok = false; break; }
 #pragma unroll
                     for (int c = 0; c < HC; ++c) {

@@ -74,12 +74,13 @@ struct CfgBS {
 };
 
 // Exponent byte of a power-of-two FP32 scale, replicated into the four bytes of a TMEM cell (one per
-// 32-element slice of the 128-K block). Anything else (sign, mantissa bits, zero) is flagged in `bad`,
+// 32-element slice of the 128-K block). Anything else (sign, mantissa bits, zero, infinity, NaN) is flagged in `bad`,
 // which the caller reports once; its exponent is used. (A per-value branch with an atomic here made
 // the scale writers the pacing loop: 476 against 358 us on 4096 x 7168 x 16384.)
 __device__ __forceinline__ uint32_t ue8m0x4(float s, uint32_t& bad) {
     const uint32_t bits = __float_as_uint(s);
-    bad |= (bits & 0x807FFFFFu) | static_cast<uint32_t>(bits == 0u);
+    // sign or mantissa bits, zero, or the all-ones exponent (infinity or NaN, which UE8M0 cannot hold)
+    bad |= (bits & 0x807FFFFFu) | static_cast<uint32_t>(bits == 0u) | static_cast<uint32_t>((bits >> 23) == 0xFFu);
     return ((bits >> 23) & 0xFFu) * 0x01010101u;
 }
 
@@ -176,7 +177,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         for (int t = unit; t < num_tiles && ok; t += num_units) {
             const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
             for (int kb = 0; kb < ti.nkb; ++kb) {
-                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 if (issuer) {
                     const int x = (ti.kb0 + kb) * BK;
@@ -200,7 +201,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         if (ok) {
             // every stage this CTA filled has been consumed before the CTA may exit
             for (int i = 0; i < STAGES && ok; ++i) {
-                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status);
+                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) ok = false;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -221,15 +222,15 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
         for (int t = unit; t < num_tiles && ok; t += num_units) {
             const TileInfo ti = decode_tile<kNormal, BN, PAIR>(p, t, nullptr, rank, srank);
             // the tile's accumulator must have been read out by the output warps
-            const bool free_acc = wait_bounded(&tmem_empty_bar[acc], aphase ^ 1u, abort_flag, p.status);
+            const bool free_acc = wait_bounded(&tmem_empty_bar[acc], aphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
             if (!__all_sync(0xffffffffu, free_acc)) { ok = false; break; }
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
             for (int kb = 0; kb < ti.nkb; ++kb) {
                 bool got = (static_cast<unsigned>(mbar_try_wait(&full_bar[stage], phase)) &
                             static_cast<unsigned>(mbar_try_wait(&sf_full_bar[slot], sphase))) != 0u;
                 if (!got)
-                    got = wait_bounded(&full_bar[stage], phase, abort_flag, p.status) &&
-                          wait_bounded(&sf_full_bar[slot], sphase, abort_flag, p.status);
+                    got = wait_bounded(&full_bar[stage], phase, abort_flag, p.status, p.wait_limit_ns) &&
+                          wait_bounded(&sf_full_bar[slot], sphase, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t a_desc = sw128_kmajor_desc(a_base + stage * C::A_BYTES);
@@ -286,7 +287,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             const float* sfb_src = p.sfb + static_cast<size_t>(min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1)) * row_stride;
             bool ok = true;
             for (int kb = 0; kb < ti.nkb; ++kb) {
-                const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status);
+                const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 float* dst = s_scales + slot * C::SLOT_FLOATS;
 #pragma unroll
@@ -326,8 +327,8 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 bool got = (static_cast<unsigned>(mbar_try_wait(&sf_empty_bar[slot], tphase ^ 1u)) &
                             static_cast<unsigned>(mbar_try_wait(&scale_full_bar[sslot], sphase))) != 0u;
                 if (!got)
-                    got = wait_bounded(&sf_empty_bar[slot], tphase ^ 1u, abort_flag, p.status) &&
-                          wait_bounded(&scale_full_bar[sslot], sphase, abort_flag, p.status);
+                    got = wait_bounded(&sf_empty_bar[slot], tphase ^ 1u, abort_flag, p.status, p.wait_limit_ns) &&
+                          wait_bounded(&scale_full_bar[sslot], sphase, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 const float* sl = s_scales + sslot * C::SLOT_FLOATS;
                 const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
@@ -363,7 +364,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             if (!ok) break;
 
             // this set's half of the tile: columns [set * BN/2, (set + 1) * BN/2)
-            const bool full = wait_bounded(&tmem_full_bar[acc], aphase, abort_flag, p.status);
+            const bool full = wait_bounded(&tmem_full_bar[acc], aphase, abort_flag, p.status, p.wait_limit_ns);
             if (!__all_sync(0xffffffffu, full)) break;
             tc_fence_after();
             const uint32_t taddr = lane_base + static_cast<uint32_t>(acc * BN);
@@ -434,7 +435,7 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             }
             if (++acc == NACC) { acc = 0; aphase ^= 1u; }
         }
-        if (bad != 0u) atomicExch(p.status, STATUS_SCALE_NOT_UE8M0);
+        if (bad != 0u) record_status(p.status, STATUS_SCALE_NOT_UE8M0);
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }

@@ -4,10 +4,10 @@
 
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "dg_kernel.cuh"
+#include "dg_tuning.h"
 
 namespace dg {
 
@@ -28,18 +28,24 @@ cudaError_t launch(const Launch& L);
 template <int BN, int PAIR>
 cudaError_t launch_bs(const Launch& L);
 
-// The swapped-operand normal GEMM for few rows (dg_inst_swap.cu).
-template <int BMT>
-cudaError_t launch_swap(const Launch& L);
+// The few-row ("decode") kernel, normal or masked layout (dg_inst_decode.cu): L.units clusters of
+// L.params.split CTAs (or CTAs, unsplit), persistent over the tiles.
+template <int MODE, int BMT>
+cudaError_t launch_decode(const Launch& L);
 
-// Programmatic dependent launch is on unless DG_PDL=0.
-inline bool pdl_enabled() {
-    static const bool on = [] {
-        const char* s = getenv("DG_PDL");
-        return !(s && s[0] == '0');
-    }();
-    return on;
-}
+// Clusters of `split` decode CTAs that can be resident at once (SMs for split 1).
+template <int MODE, int BMT>
+int decode_cluster_capacity(int split, int sms);
+
+// Tuning knobs (dg_tuning.h): the knob's value, or DG_TUNE_AUTO (-1) for the automatic choice.
+int tune(int knob);
+
+// The one-shot wait-limit fault armed by dg_testing_arm_wait_timeout (0 when none is armed); taking it
+// disarms it, so exactly one launch carries it.
+unsigned long long take_armed_wait_fault();
+
+// Programmatic dependent launch is on unless the DG_TUNE_PDL knob is 0.
+inline bool pdl_enabled() { return tune(DG_TUNE_PDL) != 0; }
 
 #ifdef DG_DEFINE_LAUNCH
 template <int MODE, int BN, int PAIR>
@@ -127,7 +133,12 @@ cudaError_t launch(const Launch& L) {
         cfg.attrs = attr;
         cfg.numAttrs += 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.tmap_d, L.params);
+    Params prm = L.params;
+    if (const unsigned long long ns = take_armed_wait_fault()) {
+        prm.wait_limit_ns = ns;
+        prm.fault_skip_first_fill = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_a, L.tmap_b, L.tmap_d, prm);
 }
 #endif
 

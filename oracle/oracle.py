@@ -8,6 +8,7 @@ scaling and higher-precision accumulation, as the DeepGEMM pages describe it.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
 import subprocess
 import threading
@@ -22,15 +23,31 @@ _lock = threading.Lock()
 _lib = None
 
 
+_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off"]
+
+
+def _digest() -> str:
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(_FLAGS).encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile ``oracle.cpp`` into ``_build/liboracle.so`` (plain g++, portable flags)."""
+    """Compile ``oracle.cpp`` into ``_build/liboracle.so`` (plain g++, portable flags); rebuilt whenever the
+    source digest differs from the one recorded beside the library."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    stamp = _LIB + ".sha256"
+    digest = _digest()
+    fresh = os.path.exists(_LIB) and os.path.exists(stamp) and open(stamp).read().strip() == digest
+    if force or not fresh:
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
-               _SRC, "-o", tmp]
-        subprocess.run(cmd, check=True)
+        subprocess.run(["g++", *_FLAGS, _SRC, "-o", tmp], check=True)
         os.replace(tmp, _LIB)
+        with open(stamp + f".tmp{os.getpid()}", "w") as f:
+            f.write(digest + "\n")
+        os.replace(stamp + f".tmp{os.getpid()}", stamp)
     return _LIB
 
 

@@ -10,12 +10,16 @@ import pytest
 import moe_grouped_gemm_tma_gb300 as dg
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "dg.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 def declared_symbols():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:dg_status|const char\*)\s+(dg_\w+)\s*\(", text, flags=re.M)))
+    syms = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = open(os.path.join(INCLUDE, h)).read()
+            syms.update(re.findall(r"^\s*(?:dg_status|const char\*|int|void)\s+(dg_\w+)\s*\(", text, flags=re.M))
+    return sorted(syms)
 
 
 def test_header_declares_every_operation():
@@ -35,6 +39,38 @@ def test_library_exports_every_declared_symbol():
 def test_python_binding_has_the_same_names():
     for s in declared_symbols():
         assert callable(getattr(dg, s)), s
+
+
+def test_tuning_knobs_set_get_and_reset():
+    dg.dg_tuning_reset()
+    assert all(dg.dg_tuning_get(k) == -1 for k in dg.TUNE_KNOBS)
+    with dg.tuning(bn=128, split=4):
+        assert dg.dg_tuning_get("bn") == 128 and dg.dg_tuning_get("split") == 4
+        assert dg.dg_tuning_get("pair") == -1
+    assert dg.dg_tuning_get("bn") == -1 and dg.dg_tuning_get("split") == -1
+    with pytest.raises(dg.DGError):
+        dg.dg_tuning_set(99, 1)
+    assert dg.load().dg_tuning_get(99) == -1
+
+
+def test_environment_is_read_only_with_the_opt_in():
+    # a stray DG_* variable must not change the product path; DG_TUNING=1 makes the library read them
+    # once, at load
+    import subprocess
+    import sys
+    code = ("import moe_grouped_gemm_tma_gb300 as dg; "
+            "print(dg.dg_tuning_get('bn'), dg.dg_tuning_get('split'), dg.dg_tuning_get('pdl'))")
+    env = dict(os.environ, DG_BN="64", DG_SPLIT="2", DG_PDL="0")
+    env.pop("DG_TUNING", None)
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, check=True)
+    assert out.stdout.split() == ["-1", "-1", "-1"]
+    env["DG_TUNING"] = "1"
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, check=True)
+    assert out.stdout.split() == ["64", "2", "0"]
+
+
+def test_wait_timeout_hook_rejects_a_zero_limit():
+    assert dg.load().dg_testing_arm_wait_timeout(0) == 1          # DG_INVALID_ARG, nothing armed
 
 
 def test_status_strings():

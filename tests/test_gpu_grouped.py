@@ -104,27 +104,52 @@ def test_masked_all_empty_and_over_max():
 
 
 @pytest.mark.parametrize("bn,pair", [(64, 1), (128, 1), (192, 1), (256, 1), (128, 2), (256, 2)])
-def test_masked_every_tile_shape(bn, pair, monkeypatch):
-    monkeypatch.setenv("DG_BN", str(bn))
-    monkeypatch.setenv("DG_PAIR", str(pair))
+def test_masked_every_tile_shape(bn, pair, tune):
+    tune(bn=bn)
+    tune(pair=pair)
     c = I.make_masked(I.seed_for(3, bn), 3, 384, 1000, 384, [300, 5, 129])
     _check_masked(c, run_masked(c), [300, 5, 129])
 
 
 @pytest.mark.parametrize("bn", [64, 128])
 @pytest.mark.parametrize("split", [2, 4, 8])
-def test_masked_split_k(bn, split, monkeypatch):
+def test_masked_split_k(bn, split, tune):
     # clusters of `split` CTAs share a tile's K blocks; one cluster per possible tile, the ones past the
     # device-side tile count have no work; an empty expert and rows past masked_m stay untouched
-    monkeypatch.setenv("DG_BN", str(bn))
-    monkeypatch.setenv("DG_SPLIT", str(split))
+    tune(bn=bn)
+    tune(split=split)
     sizes = [300, 0, 129]
     c = I.make_masked(I.seed_for(3, 100 + bn + split), 3, 384, 256, 1024, sizes)
     _check_masked(c, run_masked(c), sizes)
 
 
+@pytest.mark.parametrize("expected_m", [24, 64, 128])
+@pytest.mark.parametrize("split", [None, 1, 2, 4, 8])
+def test_masked_decode_kernel(expected_m, split, tune):
+    # the few-row (decode) kernel: tiles of 32 / 64 / 128 rows per expert from expected_m, split-K
+    # clusters of each size, an expert with more rows than a tile (several row blocks, counted on the
+    # device), an empty expert, max_m not a multiple of the tile height and N not a multiple of 128
+    tune(swap=1)
+    if split is not None:
+        tune(split=split)
+    G, max_m, N, K = 4, 300, 1000, 1024
+    sizes = [expected_m, 0, max_m, 3]
+    c = I.make_masked(I.seed_for(3, 300 + expected_m + (split or 0)), G, max_m, N, K, sizes, expected_m)
+    _check_masked(c, run_masked(c, expected_m=expected_m), sizes)
+
+
+@pytest.mark.parametrize("kernel", ["decode", "standard"])
+def test_masked_few_rows_both_kernels_agree_with_the_oracle(kernel, tune):
+    # the same decode-shaped problem through the decode kernel and through the standard masked kernel
+    tune(swap=0 if kernel == "standard" else 1)
+    sizes = [45, 64, 0, 17, 63, 1]
+    c = I.make_masked(I.seed_for(3, 77), 6, 128, 2112, 2048, sizes, 64)
+    _check_masked(c, run_masked(c, expected_m=64), sizes)
+
+
 @pytest.mark.parametrize("G,max_m,expected_m,N,K", [
     (16, 256, 64, 4096, 7168), (4, 512, 128, 7168, 2048), (1, 1024, 256, 4096, 7168), (2, 256, 256, 7168, 2048),
+    (1, 256, 64, 4096, 7168), (2, 512, 128, 7168, 2048), (4, 256, 64, 4096, 7168),
 ])
 def test_masked_workload_sampled_rows(G, max_m, expected_m, N, K):
     # the MoE decode workload at full size; every row past masked_m is sentinel-checked
@@ -146,10 +171,10 @@ def run_kgrouped(c):
 
 @pytest.mark.parametrize("bn,pair", [(0, 1), (128, 1), (192, 1), (224, 1), (256, 1), (0, 2)])
 @pytest.mark.parametrize("ks,M,N", [([256, 0, 384], 200, 264), ([128], 128, 128), ([512, 128, 1024, 256], 300, 1000)])
-def test_kgrouped_small_full_parity(ks, M, N, bn, pair, monkeypatch):
-    monkeypatch.setenv("DG_PAIR", str(pair))
+def test_kgrouped_small_full_parity(ks, M, N, bn, pair, tune):
+    tune(pair=pair)
     if bn:
-        monkeypatch.setenv("DG_BN", str(bn))
+        tune(bn=bn)
     c = I.make_kgrouped(I.seed_for(4, sum(ks) + M), len(ks), M, N, ks)
     got = run_kgrouped(c)
     want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in)

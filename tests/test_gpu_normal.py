@@ -42,11 +42,11 @@ SPECS = [(bn, 1) for bn in (64, 96, 128, 160, 192, 224, 256)] + [(bn, 2) for bn 
 
 @pytest.mark.parametrize("bn,pair", SPECS)
 @pytest.mark.parametrize("M", [200, 520])
-def test_every_tile_shape(bn, pair, M, monkeypatch):
+def test_every_tile_shape(bn, pair, M, tune):
     # ragged in M (the last row block partial; for CTA pairs also a pair whose second CTA has no rows)
     # and in N, for every tile width, single-CTA and CTA-pair tiles
-    monkeypatch.setenv("DG_BN", str(bn))
-    monkeypatch.setenv("DG_PAIR", str(pair))
+    tune(bn=bn)
+    tune(pair=pair)
     c = I.make_normal(I.seed_for(1, 900 + bn + M), M, 1000, 512)
     D = run_normal(c)
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn} pair={pair}")
@@ -54,10 +54,10 @@ def test_every_tile_shape(bn, pair, M, monkeypatch):
 
 @pytest.mark.parametrize("split", [2, 4, 8])
 @pytest.mark.parametrize("M,N,K", [(64, 1000, 4096), (128, 2112, 1024), (100, 512, 3200)])
-def test_split_k(split, M, N, K, monkeypatch):
-    # a cluster of `split` CTAs shares each tile's K blocks (unevenly when they do not divide) and
-    # reduces the partial sums through distributed shared memory
-    monkeypatch.setenv("DG_SPLIT", str(split))
+def test_split_k(split, M, N, K, tune):
+    # the standard kernel's split-K: a cluster of `split` CTAs shares each tile's K blocks (unevenly when
+    # they do not divide) and reduces the partial sums through distributed shared memory
+    tune(split=split, swap=0)
     c = I.make_normal(I.seed_for(1, 700 + split + M + N), M, N, K)
     D = run_normal(c)
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"split={split}")
@@ -118,19 +118,29 @@ def test_dense_workload_sampled_rows(N, K):
 
 @pytest.mark.parametrize("M,N,K", [
     (1, 256, 128), (17, 1000, 512), (33, 200, 384), (50, 4096, 2048), (64, 7168, 2048), (100, 2112, 1024),
-    (128, 4096, 7168), (64, 2112, 7168),
+    (128, 4096, 7168), (64, 2112, 7168), (32, 24576, 1536), (128, 32768, 512),
 ])
-def test_swapped_small_m(M, N, K, monkeypatch):
-    # the swapped-operand kernel for few rows (D^T = B . A^T on the tensor cores), with its split-K
-    # clusters, on ragged M and N
-    monkeypatch.setenv("DG_SWAP", "1")
+def test_decode_small_m(M, N, K, tune):
+    # the few-row (decode) kernel (D^T = B . A^T on the tensor cores), with the tile height and split-K
+    # clusters it picks itself, on ragged M and N
+    tune(swap=1)
     c = I.make_normal(I.seed_for(1, 500 + M + N + K), M, N, K)
     D = run_normal(c)
-    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"swapped {M}x{N}x{K}")
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"decode {M}x{N}x{K}")
 
 
-def test_swapped_integer_exact_bitwise(monkeypatch):
-    monkeypatch.setenv("DG_SWAP", "1")
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [20, 64, 120])
+def test_decode_every_split(M, split, tune):
+    # each tile height (32, 64, 128 rows) with each split-K cluster size, K blocks shared unevenly
+    tune(split=split, swap=1)
+    c = I.make_normal(I.seed_for(1, 600 + M + split), M, 1000, 1408)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"decode M={M} split={split}")
+
+
+def test_decode_integer_exact_bitwise(tune):
+    tune(swap=1)
     rng = np.random.default_rng(21)
     M, N, K = 96, 512, 512
     codes = np.array([0xB8, 0x00, 0x38], dtype=np.uint8)

@@ -21,10 +21,10 @@ def run_ue8m0(A, sfa, B, sfb, M, N):
 
 @pytest.mark.parametrize("bn", [0, 128, 192, 224, 256])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (200, 1000, 768), (1, 2112, 1024), (520, 4096, 2048)])
-def test_ue8m0_parity(M, N, K, bn, monkeypatch):
+def test_ue8m0_parity(M, N, K, bn, tune):
     # power-of-two block scales (amax/448 rounded up to a power of two); ragged M and N; every tile width
     if bn:
-        monkeypatch.setenv("DG_BN", str(bn))
+        tune(bn=bn)
     c = I.make_normal(I.seed_for(7, M + N + K), M, N, K, pow2=True)
     assert bool((torch.frexp(c.sfa)[0] == 0.5).all()) and bool((torch.frexp(c.sfb)[0] == 0.5).all())
     D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
@@ -55,20 +55,31 @@ def test_ue8m0_reports_non_power_of_two_scales():
     assert dg.dg_device_status() == 0                       # reported once, then cleared
 
 
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")])
+def test_ue8m0_reports_infinite_or_nan_scale(bad):
+    # an exponent byte of all ones is not a power of two that UE8M0 can hold (it stands for NaN there)
+    c = I.make_normal(I.seed_for(7, 3), 128, 256, 256, pow2=True)
+    sfa = c.sfa.clone()
+    sfa[5, 1] = bad
+    run_ue8m0(c.A, sfa, c.B, c.sfb, 128, 256)
+    assert dg.dg_device_status() == 7
+    assert dg.dg_device_status() == 0
+
+
 @pytest.mark.parametrize("split", [2, 4, 8])
 @pytest.mark.parametrize("M,N,K", [(64, 1000, 3200), (100, 2112, 1024)])
-def test_ue8m0_split_k(split, M, N, K, monkeypatch):
+def test_ue8m0_split_k(split, M, N, K, tune):
     # a cluster of `split` CTAs shares each tile's K blocks (unevenly when they do not divide); each
     # accumulates its range in TMEM and the FP32 partials are reduced through distributed shared memory
-    monkeypatch.setenv("DG_SPLIT", str(split))
+    tune(split=split)
     c = I.make_normal(I.seed_for(7, 50 + split + M), M, N, K, pow2=True)
     D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
     assert dg.dg_device_status() == 0
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 split={split} {M}x{N}x{K}")
 
 
-def test_ue8m0_split_k_reports_non_power_of_two_scales(monkeypatch):
-    monkeypatch.setenv("DG_SPLIT", "4")
+def test_ue8m0_split_k_reports_non_power_of_two_scales(tune):
+    tune(split=4)
     c = I.make_normal(I.seed_for(7, 2), 64, 512, 2048)
     run_ue8m0(c.A, c.sfa, c.B, c.sfb, 64, 512)
     assert dg.dg_device_status() == 7
@@ -76,19 +87,19 @@ def test_ue8m0_split_k_reports_non_power_of_two_scales(monkeypatch):
 
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("M,N,K", [(200, 1000, 768), (520, 4096, 2048), (256, 264, 384)])
-def test_ue8m0_cta_pairs(M, N, K, bn, monkeypatch):
+def test_ue8m0_cta_pairs(M, N, K, bn, tune):
     # 256-row tiles over a CTA pair (cta_group::2): each CTA writes the exponents of its own rows and all
     # of B's; ragged M leaves the second CTA of the last pair partly or wholly past M
-    monkeypatch.setenv("DG_PAIR", "2")
-    monkeypatch.setenv("DG_BN", str(bn))
+    tune(pair=2)
+    tune(bn=bn)
     c = I.make_normal(I.seed_for(7, 70 + bn + M), M, N, K, pow2=True)
     D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, M, N)
     assert dg.dg_device_status() == 0
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 pair BN={bn} {M}x{N}x{K}")
 
 
-def test_ue8m0_cta_pairs_integer_exact_bitwise(monkeypatch):
-    monkeypatch.setenv("DG_PAIR", "2")
+def test_ue8m0_cta_pairs_integer_exact_bitwise(tune):
+    tune(pair=2)
     rng = np.random.default_rng(17)
     M, N, K = 512, 384, 512
     codes = np.array([0xB8, 0x00, 0x38], dtype=np.uint8)
