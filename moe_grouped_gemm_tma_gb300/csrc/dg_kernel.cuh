@@ -176,6 +176,12 @@ struct Cfg {
     // are issued and waited on once, and the accumulator is released before any FMA, which keeps the
     // promotion arithmetic off the two-accumulator MMA -> release -> MMA loop.
     static constexpr bool EPI_ONE = MODE != kKGrouped && COLS <= 96;
+    // Wide tiles outside the k-grouped layout read their two scales per K block straight from global
+    // memory (L1-resident after a tile's first block), one block ahead, instead of from the scale
+    // stager's slots: that takes a barrier round trip per block off the epilogue and leaves the stager
+    // warp idle, whose issue slots the epilogue warps of its sub-partition then get (per-block clock
+    // stamps showed those warps releasing the accumulator last).
+    static constexpr bool DIRECT_SCALES = !KPAR && MODE != kKGrouped;
     static constexpr int EPI_GC = EPI_ONE ? CHUNKS : ((MODE == kKGrouped && COLS > 96) ? 1 : 2);
     static constexpr bool EPI_DB = !EPI_ONE;
     // split-K partial sums: [128 rows][BN + 4] FP32 (padded rows: conflict-free 16-byte stores), in the
@@ -607,7 +613,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 }
             }
             if (!ok && any && issuer) drain_wait(&tmem_full_bar[last_acc], last_parity);
-        } else if (warp == 2) {
+        } else if (warp == 2 && !C::DIRECT_SCALES) {
             // ------------------------------------------------------------------ scale stager
             int slot = 0;
             uint32_t sphase = 0;
@@ -687,7 +693,62 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 #pragma unroll
             for (int j = 0; j < COLS; ++j) accum[j] = 0.f;
 
-            if constexpr (!C::KPAR) {
+            if constexpr (C::DIRECT_SCALES) {
+                // sfa of this thread's row and the sfb of its (at most two) 128-column blocks, read one K
+                // block ahead
+                const int a_rows_total = (MODE == kMasked) ? p.groups * p.rows : p.rows;
+                const float* sfa_row = p.sfa + static_cast<size_t>(min(ti.a_row + row_in_tile, a_rows_total - 1)) * p.kbs + ti.kb0;
+                const float* sfb_0 = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + min(cstart / 128, p.sfb_rows - 1)) * p.kbs + ti.kb0;
+                const float* sfb_1 = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + min(cstart / 128 + 1, p.sfb_rows - 1)) * p.kbs + ti.kb0;
+                float sa_n = __ldg(sfa_row), b0_n = __ldg(sfb_0), b1_n = __ldg(sfb_1);
+                // Each K block's TMEM loads in two halves: the first half is loaded and promoted, then the
+                // second half is loaded and the accumulator released before its FMAs, so the MMA of block
+                // kb + NACC waits for half a block's FMAs instead of three quarters (EPI_ONE tiles load the
+                // whole block before any FMA).
+                constexpr int H1 = C::EPI_ONE ? CHUNKS : (CHUNKS + 1) / 2;
+                constexpr int H2 = CHUNKS - H1;
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    const float sa = sa_n, b0 = b0_n, b1 = b1_n;
+                    if (kb + 1 < ti.nkb) {
+                        sa_n = __ldg(sfa_row + kb + 1);
+                        b0_n = __ldg(sfb_0 + kb + 1);
+                        b1_n = __ldg(sfb_1 + kb + 1);
+                    }
+                    bool got = mbar_try_wait(&tmem_full_bar[acc], acc_phase);
+                    if (!got) got = wait_bounded(&tmem_full_bar[acc], acc_phase, abort_flag, p.status, p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t taddr = lane_addr + static_cast<uint32_t>(acc * BN);
+                    const float s0 = sa * b0, s1 = sa * b1;
+                    uint32_t rb[H1][16];
+#pragma unroll
+                    for (int c = 0; c < H1; ++c) tmem_ld_x16(taddr + c * 16, rb[c]);
+                    tmem_ld_wait();
+                    if constexpr (H2 > 0) {
+#pragma unroll
+                        for (int c = 0; c < H1; ++c) promote_chunk<MODE, COLS>(accum, rb[c], c, (c < split) ? s0 : s1, sa, nullptr);
+#pragma unroll
+                        for (int c = 0; c < H2; ++c) tmem_ld_x16(taddr + (H1 + c) * 16, rb[c]);
+                        tmem_ld_wait();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // the accumulator is released on the leader's barrier (the peer's is unused)
+                        if (PAIR == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty_bar[acc]), 0));
+                        else mbar_arrive(&tmem_empty_bar[acc]);
+                    }
+                    if constexpr (H2 > 0) {
+#pragma unroll
+                        for (int c = 0; c < H2; ++c)
+                            promote_chunk<MODE, COLS>(accum, rb[c], H1 + c, (H1 + c < split) ? s0 : s1, sa, nullptr);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < H1; ++c) promote_chunk<MODE, COLS>(accum, rb[c], c, (c < split) ? s0 : s1, sa, nullptr);
+                    }
+                    if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
+                }
+            } else if constexpr (!C::KPAR) {
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     // both barriers are probed at once (each try_wait is a round trip to shared memory);
                     // only an incomplete one falls back to the bounded waits

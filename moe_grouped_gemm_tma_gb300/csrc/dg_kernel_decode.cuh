@@ -49,8 +49,7 @@ struct CfgDec {
     static constexpr int STATIC_RESERVE = 640 + 4 * (MAX_MASKED_G + 1);
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES, 0, STATIC_RESERVE);
     static constexpr int DYN_SMEM = 1024 + STAGES * STAGE_BYTES + SCALE_BYTES;
-    static constexpr int PSTRIDE = BMT + 4;              // split-K partials [128][BMT + 4] in the ring
-    static constexpr int PARTIAL_BYTES = BNT * PSTRIDE * 4;
+    static constexpr int PARTIAL_BYTES = BMT * BNT * 4;  // split-K partials [BMT rows][128 columns] in the ring
     static_assert(PARTIAL_BYTES <= STAGES * STAGE_BYTES, "split-K partials must fit in the operand ring");
     static_assert(STAGES >= 2, "not enough shared memory for two stages");
     static_assert(HALF % 16 == 0, "each warpgroup loads whole 16-column chunks");
@@ -114,6 +113,7 @@ dg_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     constexpr int SG = C::SGROUPS;
     constexpr int HALF = C::HALF;
     constexpr int HCH = HALF / 16;                        // 16-column TMEM loads per K block and thread
+    constexpr int LB = (HALF + KG * HALF > 160) ? 1 : KG; // K blocks per batch of TMEM loads
     constexpr uint32_t IDESC = idesc_e4m3_f32(128, BMT);
 
     extern __shared__ uint8_t dyn_smem[];
@@ -217,8 +217,12 @@ dg_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             if (warp == 0) {
                 // ------------------------------------------------------------ TMA producer
                 for (int kb = 0; kb < ti.nkb && ok; ++kb) {
-                    const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    // a stage never filled before is free: the first pass over the ring issues its loads
+                    // without a barrier round trip
+                    if (issued & (1u << stage)) {
+                        const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    }
                     if (issuer) {
                         const int x = (ti.kb0 + kb) * BK;
                         mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
@@ -282,19 +286,35 @@ dg_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 }
             }
             if (split_k) {
+                if (warp == 0 && ok) {
+                    // every stage of this tile has been consumed (its MMAs have completed) before the
+                    // ring holds partial sums; this also leaves no MMA-completion arrival in flight
+                    // when the CTA exits after its last tile. The ring position is not advanced: the
+                    // wait is the one the next refill of each stage would make.
+                    int s = stage;
+                    uint32_t ph = phase;
+                    for (int i = 0; i < STAGES && ok; ++i) {
+                        const bool got = wait_bounded(&empty_bar[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, got)) ok = false;
+                        if (++s == STAGES) { s = 0; ph ^= 1u; }
+                    }
+                }
                 // the epilogue warps park, reduce and store between these two barriers
                 cluster_sync();
                 cluster_sync();
             }
         }
         // ------------------------------------------------------------------ drain
-        if (warp == 0 && ok) {
+        if (warp == 0 && ok && !split_k) {
             // every stage this CTA filled has been consumed, so no MMA-completion arrival is still in
-            // flight towards this CTA when it exits
+            // flight towards this CTA when it exits (split-K tiles drained the ring before their
+            // reduction already)
+            int s = stage;
+            uint32_t ph = phase;
             for (int i = 0; i < STAGES && ok; ++i) {
-                const bool got = wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                const bool got = wait_bounded(&empty_bar[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) ok = false;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
         if (warp == 0 && !ok && issuer) {
@@ -329,33 +349,41 @@ dg_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                           wait_bounded(&scale_full_bar[sslot], sphase, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 tc_fence_after();
-                // the whole group's partials of this thread's rows, one wait for all loads
-                uint32_t r[KG][HCH][16];
-#pragma unroll
-                for (int j = 0; j < KG; ++j)
-#pragma unroll
-                    for (int c = 0; c < HCH; ++c)
-                        if (j < ng) tmem_ld_x16(lane_addr + static_cast<uint32_t>((grp * KG + j) * BMT + c * 16), r[j][c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tmem_empty_bar[grp]);
+                // the group's partials of this thread's rows in batches of LB K blocks (the whole group
+                // at once unless the registers do not hold it), one wait per batch; the accumulators are
+                // released once the last batch is in registers, before its FMAs
                 const float* sl = s_scales + sslot * C::SLOT_FLOATS;
 #pragma unroll
-                for (int j = 0; j < KG; ++j) {
-                    if (j < ng) {
-                        const float sb = sl[j * C::SROW + BMT];
-                        const float* sa = sl + j * C::SROW + h * HALF;
+                for (int jb = 0; jb < KG; jb += LB) {
+                    if (jb >= ng) break;
+                    uint32_t r[LB][HCH][16];
 #pragma unroll
-                        for (int c = 0; c < HCH; ++c) {
+                    for (int j = 0; j < LB; ++j)
 #pragma unroll
-                            for (int e = 0; e < 16; e += 4) {
-                                const float4 s4 = *reinterpret_cast<const float4*>(sa + c * 16 + e);
-                                const int m = c * 16 + e;
-                                acc[m + 0] = fmaf(__uint_as_float(r[j][c][e + 0]), s4.x * sb, acc[m + 0]);
-                                acc[m + 1] = fmaf(__uint_as_float(r[j][c][e + 1]), s4.y * sb, acc[m + 1]);
-                                acc[m + 2] = fmaf(__uint_as_float(r[j][c][e + 2]), s4.z * sb, acc[m + 2]);
-                                acc[m + 3] = fmaf(__uint_as_float(r[j][c][e + 3]), s4.w * sb, acc[m + 3]);
+                        for (int c = 0; c < HCH; ++c)
+                            if (jb + j < ng) tmem_ld_x16(lane_addr + static_cast<uint32_t>((grp * KG + jb + j) * BMT + c * 16), r[j][c]);
+                    tmem_ld_wait();
+                    if (jb + LB >= ng) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tmem_empty_bar[grp]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < LB; ++j) {
+                        if (jb + j < ng) {
+                            const float sb = sl[(jb + j) * C::SROW + BMT];
+                            const float* sa = sl + (jb + j) * C::SROW + h * HALF;
+#pragma unroll
+                            for (int c = 0; c < HCH; ++c) {
+#pragma unroll
+                                for (int e = 0; e < 16; e += 4) {
+                                    const float4 s4 = *reinterpret_cast<const float4*>(sa + c * 16 + e);
+                                    const int m = c * 16 + e;
+                                    acc[m + 0] = fmaf(__uint_as_float(r[j][c][e + 0]), s4.x * sb, acc[m + 0]);
+                                    acc[m + 1] = fmaf(__uint_as_float(r[j][c][e + 1]), s4.y * sb, acc[m + 1]);
+                                    acc[m + 2] = fmaf(__uint_as_float(r[j][c][e + 2]), s4.z * sb, acc[m + 2]);
+                                    acc[m + 3] = fmaf(__uint_as_float(r[j][c][e + 3]), s4.w * sb, acc[m + 3]);
+                                }
                             }
                         }
                     }
@@ -367,13 +395,13 @@ dg_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             }
             if (ok) {
                 if (split_k) {
-                    // park this CTA's partial sums [column n][row m] in the operand ring: every stage of
+                    // park this CTA's partial sums [row m][column n] in the operand ring (every stage of
                     // the tile has been consumed by an MMA that has completed, and the producer issues
-                    // nothing more before the second cluster barrier below
-                    float* prow = reinterpret_cast<float*>(smem) + n_in_tile * C::PSTRIDE + h * HALF;
+                    // nothing more before the second cluster barrier below): a warp writes 128
+                    // contiguous bytes per row, and each CTA's share of rows is one contiguous block
+                    float* pcol = reinterpret_cast<float*>(smem) + (h * HALF) * C::BNT + n_in_tile;
 #pragma unroll
-                    for (int m = 0; m < HALF; m += 4)
-                        *reinterpret_cast<float4*>(prow + m) = make_float4(acc[m], acc[m + 1], acc[m + 2], acc[m + 3]);
+                    for (int m = 0; m < HALF; ++m) pcol[m * C::BNT] = acc[m];
                 } else {
                     // column n of D for this warpgroup's rows: a warp writes 64 contiguous bytes per row
                     const int n = ti.n0 + n_in_tile;
@@ -390,28 +418,25 @@ dg_decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             }
             if (split_k) {
                 // ------------------------------------------------------------ split-K reduction
-                // every CTA's partials are visible cluster-wide after this barrier; CTA s reduces columns
-                // [s*128/S, (s+1)*128/S) of the tile over all S partials in fixed order (s = 0..S-1) and
-                // stores BF16; the second barrier keeps every CTA's ring untouched until all remote reads
-                // are done (only then does the producer refill it with the next tile)
+                // every CTA's partials are visible cluster-wide after this barrier; CTA s reduces rows
+                // [s*BMT/S, (s+1)*BMT/S) of the tile, a contiguous block of every CTA's partials read
+                // with consecutive threads on consecutive 16-byte chunks, over all S partials in fixed
+                // order (s = 0..S-1), and stores BF16 rows (8 bytes a thread, a warp 256 contiguous
+                // bytes); the second barrier keeps every CTA's ring untouched until all remote reads are
+                // done (only then does the producer refill it with the next tile)
                 cluster_sync();
                 if (!*abort_flag) {
-                    const int cols_per = 128 / p.split;
-                    const int groups = cols_per * (BMT / 4);
+                    const int rows_per = BMT / p.split;
+                    const int chunks = rows_per * (C::BNT / 4);
                     const uint32_t part_local = smem_u32(smem);
-                    for (int gi = static_cast<int>(threadIdx.x) - EPI_WARP0 * 32; gi < groups; gi += EPI_WARPS * 32) {
-                        const int col = srank * cols_per + gi % cols_per;
-                        const int r4 = (gi / cols_per) * 4;
-                        const uint32_t off = static_cast<uint32_t>((col * C::PSTRIDE + r4) * 4);
-                        const float4 sum = cluster_sum_v4(part_local + off, p.split);
-                        const int n = ti.n0 + col;
-                        if (n < p.n) {
-                            __nv_bfloat16* dcol = reinterpret_cast<__nv_bfloat16*>(p.d) + n;
-                            const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                if (r4 + i < ti.rows_valid)
-                                    dcol[static_cast<size_t>(ti.a_row + r4 + i) * p.n] = __float2bfloat16_rn(vals[i]);
+                    for (int f = static_cast<int>(threadIdx.x) - EPI_WARP0 * 32; f < chunks; f += EPI_WARPS * 32) {
+                        const int m = srank * rows_per + f / (C::BNT / 4);
+                        const int n4 = (f % (C::BNT / 4)) * 4;
+                        const float4 sum = cluster_sum_v4(part_local + static_cast<uint32_t>((m * C::BNT + n4) * 4), p.split);
+                        if (m < ti.rows_valid && ti.n0 + n4 < p.n) {
+                            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) +
+                                                 static_cast<size_t>(ti.a_row + m) * p.n + ti.n0 + n4;
+                            st_global_v2(dst, pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
                         }
                     }
                 }
