@@ -172,6 +172,12 @@ struct Cfg {
     // already: a pass costs several hundred cycles of barrier round trips, more than the MMA of a narrow
     // block. (Measured: it slows the wide two-accumulator tiles of the other layouts.)
     static constexpr bool KB_PAIRING = (NACC >= 4) || MODE == kKGrouped;
+    // MMA issue takes issue slots from the epilogue warps on the issuing warp's sub-partition (per-block
+    // clock stamps: those two warps released each accumulator ~350 cycles after the other six, and
+    // moving the issuer to another warp moved the lag with it). Where the accumulators pair up (an even
+    // count, one K block per pass), two warps on different sub-partitions share the issue: warp 1 the
+    // even accumulators, warp 3 the odd ones.
+    static constexpr int MMA_WARPS = (!KB_PAIRING && NACC % 2 == 0) ? 2 : 1;
     // Up to 96 columns a thread, a whole K block fits in registers beside the running sums: all its loads
     // are issued and waited on once, and the accumulator is released before any FMA, which keeps the
     // promotion arithmetic off the two-accumulator MMA -> release -> MMA loop.
@@ -292,6 +298,31 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit) {
+            *abort_flag = 1;
+            record_status(status, STATUS_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for the control warps (TMA producer, MMA issuers): between polls the warp sleeps
+// briefly, so that a control warp waiting on a barrier takes no issue slots from the two epilogue warps
+// that share its sub-partition (per-block clock stamps: a control warp waiting with try_wait alone
+// delayed those warps' accumulator release by ~350 cycles per K block). Same result and bound as
+// wait_bounded; the reaction to a completed phase is at most one sleep later.
+__device__ __forceinline__ bool wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             int* status, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit = limit_ns ? limit_ns : WAIT_LIMIT_NS;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i) {
+            if (mbar_test_wait(bar, parity)) return true;
+            __nanosleep(32);
+        }
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > limit) {
             *abort_flag = 1;
@@ -486,7 +517,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
                     const bool f0 = mbar_try_wait(&empty_bar[stage], phase ^ 1u);
                     const bool f1 = more && mbar_test_wait(&empty_bar[s1], ph1 ^ 1u);
-                    const bool got = f0 || wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                    const bool got = f0 || wait_backoff(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
                     for (int j = 0; j < take; ++j) {
@@ -542,11 +573,14 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 for (int s = 0; s < STAGES; ++s)
                     if (issued & (1u << s)) drain_wait(&full_bar[s], (issued_parity >> s) & 1u);
             }
-        } else if (warp == 1 && leader) {
+        } else if ((warp == 1 || (C::MMA_WARPS == 2 && warp == 3)) && leader) {
             // ------------------------------------------------------------------ MMA issuer
             // The whole warp runs the loop so descriptors and TMEM addresses are warp-uniform (kept in
-            // uniform registers); one elected lane issues the MMAs and commits.
+            // uniform registers); one elected lane issues the MMAs and commits. With two issuing warps
+            // (see Cfg::MMA_WARPS) warp 1 takes the K blocks of the even accumulators and warp 3 those of
+            // the odd ones; each walks every block to keep the ring positions.
             const bool issuer = elect_one();
+            const int mine = (warp == 3) ? 1 : 0;
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
@@ -557,6 +591,13 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
                 for (int kb = 0; kb < ti.nkb;) {
+                    if (C::MMA_WARPS == 2 && (acc & 1) != mine) {
+                        // the other issuing warp's block: only the ring positions move
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                        if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
+                        ++kb;
+                        continue;
+                    }
                     // This K block's accumulator and stage and, when the tile has another K block, the
                     // next ones are probed at once; the second block is issued in the same pass only if it
                     // is ready already (never waited for, so a two-accumulator tile keeps its overlap).
