@@ -472,17 +472,20 @@ static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B,
     Launch L;
     std::memset(&L, 0, sizeof(L));
     const int kbs = K / 128;
-    // Few rows with a long K per CTA: the decode kernel (swapped operands, K-block groups, split-K
-    // clusters sized to fill the SMs). With short K per CTA its per-tile set-up and reduction cost more
-    // than its fuller stages save, and the standard kernel with split-K is faster (measured: 64 x 7168 x
-    // 16384 35.0 against 43.7 us; 64 x 2112 x 7168 18.6 against 14.5 us). The DG_TUNE_SWAP knob forces
-    // the choice (1 = decode kernel, 0 = standard kernel).
+    // Few rows, long K, 32..64 column tiles of 128: the decode kernel (swapped operands, K-block groups,
+    // split-K clusters sized to fill the SMs). Measured in-stream against the standard kernel with
+    // split-K, fraction of the HBM roofline: 64 x 7168 x 16384 0.55 against 0.45, 64 x 4096 x 7168 0.35
+    // against 0.31. Outside that range the standard kernel was as fast or faster (64 x 2112 x 7168,
+    // 17 column tiles: 0.20 against 0.22; 128-row tiles: 128 x 7168 x 16384 0.44 against 0.46; short K
+    // or 192..256 column tiles: 0.22-0.37 against 0.26-0.52). The DG_TUNE_SWAP knob forces the choice
+    // (1 = decode kernel, 0 = standard kernel).
     DecodePlan pl;
     bool decode = false;
     if (!a_mn && !b_mn && !pair && M <= 128 && tune(DG_TUNE_BN) < 0) {
-        pl = plan_decode<kNormal>(1, M, M, N, kbs, dev.sms);
-        decode = cdiv(kbs, pl.split) >= 32;
+        const int col_tiles = cdiv(N, 128);
+        decode = M <= 64 && K >= 7168 && col_tiles >= 32 && col_tiles <= 64;
         if (const int v = tune(DG_TUNE_SWAP); v >= 0) decode = (v == 1);
+        if (decode) pl = plan_decode<kNormal>(1, M, M, N, kbs, dev.sms);
     }
     if (decode) {
         if (make_operand_map(&L.tmap_a, A, M, K, pl.bmt) != DG_OK) return DG_CUDA_ERROR;
@@ -527,6 +530,11 @@ static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B,
     p.split = split;
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
+    // Long K: a band's A row blocks (2 MB each at K = 16384) are evicted before the band's next round of
+    // tiles reads them again, unless A is marked evict-last and B (read only by tiles in flight
+    // together) evict-first. Measured on 4096 x 7168 x 16384: DRAM traffic per launch 483 -> 355 MB
+    // (algorithmic 243 MB), 330.6 -> 325.7 us; on K <= 7168 shapes it measured 0.5-1.5% slower.
+    p.l2_hint = (!a_mn && !b_mn && K >= 8192) ? 1 : 0;
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);
@@ -740,10 +748,17 @@ dg_status dg_m_grouped_masked(const uint8_t* A, const float* sfa, const uint8_t*
     if (st != DG_OK) return st;
 
     const int hint = (expected_m > 0 && expected_m < max_m) ? expected_m : max_m;
-    if (hint <= 128 && tune(DG_TUNE_SWAP) == 1 && tune(DG_TUNE_PAIR) != 2 && tune(DG_TUNE_BN) < 0) {
-        // Decode: few rows per expert. The decode kernel (swapped operands: B's rows fill the MMA's 128
-        // lanes, the tokens are its N) counts each expert's row blocks on the device from masked_m; the
-        // plan (tile height, split-K) follows expected_m, and any masked_m up to max_m stays correct.
+    // Decode with few tiles (a single expert of up to 128 expected rows, long K): the decode kernel.
+    // Measured in-stream, fraction of the HBM roofline, one expert, N = 4096, K = 7168: 0.32 against 0.26
+    // (expected_m = 64) and 0.28 against 0.23 (128). With more experts, or short K, the standard kernel
+    // was as fast or faster (G = 2..16: 0.39-0.73 against 0.44-0.85). DG_TUNE_SWAP forces the choice.
+    bool decode = hint <= 128 && K >= 7168 &&
+                  static_cast<int64_t>(G) * cdiv(hint, hint <= 32 ? 32 : (hint <= 64 ? 64 : 128)) * cdiv(N, 128) <= 32;
+    if (const int v = tune(DG_TUNE_SWAP); v >= 0) decode = (v == 1) && hint <= 128;
+    if (decode && tune(DG_TUNE_PAIR) != 2 && tune(DG_TUNE_BN) < 0) {
+        // The decode kernel (swapped operands: B's rows fill the MMA's 128 lanes, the tokens are its N)
+        // counts each expert's row blocks on the device from masked_m; the plan (tile height, split-K)
+        // follows expected_m, and any masked_m up to max_m stays correct.
         const DecodePlan pl = plan_decode<kMasked>(G, hint, max_m, N, K / 128, dev.sms);
         Launch L;
         std::memset(&L, 0, sizeof(L));

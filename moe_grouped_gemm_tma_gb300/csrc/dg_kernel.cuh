@@ -94,6 +94,7 @@ struct Params {
     int a_mn, b_mn;            // normal layout: A stored [K, M] / B stored [K, N] (MN-major operands)
     int sf_packed;             // block-scaled: sfa / sfb hold UE8M0 exponents, four K blocks per int32
     int sf_words;              // block-scaled, packed: int32 words per scale row, ceil(kbs / 4)
+    int l2_hint;               // normal layout, long K: A loads evict-last, B loads evict-first in L2
     unsigned long long wait_limit_ns;  // bound of every wait (0 = WAIT_LIMIT_NS); tests shorten it
     int fault_skip_first_fill;  // test only (0 in every product call): the producer leaves its first
                                 // stage unfilled, so the MMA issuer's wait on it runs out
@@ -503,6 +504,10 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             uint32_t issued = 0, issued_parity = 0;   // per-stage bits, for the abort drain
             bool ok = true;
             bool skip_fill = p.fault_skip_first_fill != 0;   // test only: leave the first stage empty
+            // L2 policies for the long-K normal layout: a band's A row blocks are read again by the next
+            // round of tiles, B's column blocks only by tiles in flight at the same time
+            const uint64_t pol_a = policy_evict_last(), pol_b = policy_evict_first();
+            const bool hint = (MODE == kNormal && PAIR == 1 && p.l2_hint != 0);
             for (int t = unit; t < num_tiles && ok; t += num_units) {
                 const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
                 if (!ti.valid) continue;
@@ -537,10 +542,13 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                                 // MN-major operands: boxes of 128 M (N) bytes x 128 k rows; B takes one
                                 // box per 128 columns of the tile (the host allows it for BN % 128 == 0)
                                 if ((MODE == kNormal && p.a_mn)) tma_load_2d(&tmap_a, &full_bar[stage], a_dst, ti.a_row, x);
+                                else if (hint) tma_load_2d_hint(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row, pol_a);
                                 else tma_load_2d(&tmap_a, &full_bar[stage], a_dst, x, ti.a_row);
                                 if ((MODE == kNormal && p.b_mn)) {
                                     for (int j = 0; j < C::B_ROWS / 128; ++j)
                                         tma_load_2d(&tmap_b, &full_bar[stage], b_dst + j * (128 * BK), ti.b_row + 128 * j, x);
+                                } else if (hint) {
+                                    tma_load_2d_hint(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row, pol_b);
                                 } else {
                                     tma_load_2d(&tmap_b, &full_bar[stage], b_dst, x, ti.b_row);
                                 }

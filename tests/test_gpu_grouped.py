@@ -237,9 +237,11 @@ def test_dense_wgrad_k_zero():
     assert bool((D == 0.0).all())          # the empty product, stored
 
 
-def test_masked_replayed_from_a_cuda_graph():
+@pytest.mark.parametrize("kernel", ["standard", "decode"])
+def test_masked_replayed_from_a_cuda_graph(kernel, tune):
     # decode runs the masked layout under CUDA graphs: one capture, replayed with new per-expert counts
     # written into the same device buffer; every argument the host sees stays fixed
+    tune(swap=1 if kernel == "decode" else 0)
     G, max_m, N, K = 4, 256, 1024, 512
     first = [100, 0, 256, 37]
     c = I.make_masked(I.seed_for(3, 900), G, max_m, N, K, first, 128)
