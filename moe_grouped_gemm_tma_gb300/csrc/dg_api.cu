@@ -157,19 +157,6 @@ dg_status make_tile_output_map(CUtensorMap* m, void* base, int64_t rows, int64_t
     return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
 }
 
-// FP32 weight gradient [G][M][N] (N contiguous) added into in boxes of 1 x 32 rows x 8 columns (32
-// bytes) with the 32-byte swizzle; the third dimension keeps each box inside its expert's M rows.
-dg_status make_wgrad_map(CUtensorMap* m, float* base, int64_t g, int64_t rows, int64_t n) {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(g)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(n) * 4, static_cast<cuuint64_t>(rows * n) * 4};
-    cuuint32_t box[3] = {8u, 32u, 1u};
-    cuuint32_t es[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
-                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? DG_OK : DG_CUDA_ERROR;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
@@ -407,7 +394,6 @@ static dg_status wgrad_impl(const uint8_t* A, const float* sfa, const uint8_t* B
     std::memset(&L, 0, sizeof(L));
     if (make_operand_map(&L.tmap_a, A, M, sumK, BM) != DG_OK) return DG_CUDA_ERROR;
     if (make_operand_map(&L.tmap_b, B, N, sumK, bn / sp.pair) != DG_OK) return DG_CUDA_ERROR;
-    if (make_wgrad_map(&L.tmap_d, D, G, M, N) != DG_OK) return DG_CUDA_ERROR;
     Params& p = L.params;
     p.sfa = sfa;
     p.sfb = sfb;

@@ -66,6 +66,9 @@ constexpr int TMEM_COLS = 512;
 constexpr int SCALE_SLOTS_MAX = 16;
 constexpr int MAX_MASKED_G = 1024;
 constexpr int MAX_KGROUPS = 128;
+// k-grouped: K blocks per scale patch the stager loads in one pass (a power of two dividing 32 and the
+// scale ring's slot count)
+constexpr int KG_PATCH = 4;
 constexpr int SMEM_LIMIT = 232448;      // 227 KB per CTA on sm_100-family parts
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 50000000ull;
@@ -120,7 +123,9 @@ struct Cfg {
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // scale slot: sfa of the CTA's 128 rows, then sfb: 4 block rows (from n0/128), or BN per-row values
-    static constexpr int SB = (MODE == kKGrouped) ? BN : 4;
+    // (k-grouped slots are padded by 8 floats, so that the stager's patch writes -- 8 rows or columns x
+    // 4 consecutive slots per instruction -- fall in distinct banks)
+    static constexpr int SB = (MODE == kKGrouped) ? BN + 8 : 4;
     static constexpr int SLOT_FLOATS = BM + SB;
     // the k-grouped slots hold BN per-column values, so they get a shallower ring (eight: six would
     // leave room for a fifth operand stage at BN = 192, but the stager's scattered per-column loads
@@ -150,12 +155,13 @@ struct Cfg {
     // (each epilogue warp its 32 rows x COLS columns as boxes of 32 x 32 with the 64-byte swizzle),
     // written by TMA stores that the warp does not wait for until it stages its next tile (a tile's
     // 64 KB take the SM's store path several thousand cycles, which would otherwise stall promotion).
-    // Otherwise 2 KB per epilogue warp: for the k-grouped FP32 output STORE_SLOTS TMA boxes of 32 rows x
-    // 8 columns in flight; for BF16 out one buffer of 32 rows x 32 columns, written with plain stores.
-    static constexpr int STORE_SLOTS = 2;
+    // Otherwise 2 KB per epilogue warp: for the k-grouped FP32 output a buffer of 32 rows x 16 columns
+    // that turns each lane's row into coalesced vector reductions; for BF16 out one buffer of 32 rows x
+    // 32 columns, written with plain stores. (Shared memory is kept small for the k-grouped layout: its
+    // scale stager relies on what L1 keeps beside it.)
     static constexpr bool FULL_STAGE = MODE != kKGrouped && COLS % 32 == 0 &&
         ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, BM * BN * 2, STATIC_RESERVE) >= 4;
-    static constexpr int STORE_WARP_BYTES = FULL_STAGE ? 32 * COLS * 2 : STORE_SLOTS * 1024;
+    static constexpr int STORE_WARP_BYTES = FULL_STAGE ? 32 * COLS * 2 : 2048;
     static constexpr int STORE_BYTES = EPI_WARPS_C * STORE_WARP_BYTES;
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
@@ -674,40 +680,71 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     sfa_rows[i] = p.sfa + static_cast<size_t>(min(ti.a_row + lane + 32 * i, a_rows_total - 1)) * p.kbs + ti.kb0;
-                const float* sfb_src;
-                if (MODE == kKGrouped) {
-                    sfb_src = p.sfb + ti.kb0;   // row n: + n * kbs
-                } else {
-                    const int blk = min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1);
-                    sfb_src = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + blk) * p.kbs + ti.kb0;
-                }
+                const int blk = min(ti.n0 / 128 + (lane & 3), p.sfb_rows - 1);
+                const float* sfb_src = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + blk) * p.kbs + ti.kb0;
                 bool ok = true;
-                for (int kb = 0; kb < ti.nkb;) {
-                    // as in the producer: a second slot is filled in the same pass if it is free already
-                    int s1 = slot + 1;
-                    uint32_t sp1 = sphase;
-                    if (s1 == C::SCALE_SLOTS) { s1 = 0; sp1 ^= 1u; }
-                    const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
-                    const bool f0 = mbar_try_wait(&scale_empty_bar[slot], sphase ^ 1u);
-                    const bool f1 = more && mbar_test_wait(&scale_empty_bar[s1], sp1 ^ 1u);
-                    const bool got = f0 || wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
-                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
-                    for (int j = 0; j < take; ++j) {
-                        const int k = kb + j;
-                        float* dst = s_scales + slot * C::SLOT_FLOATS;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + k);
-                        if (MODE == kKGrouped) {
-                            for (int c = lane; c < BN; c += 32)
-                                cp_async_4(dst + BM + c, sfb_src + static_cast<size_t>(min(ti.n0 + c, p.n - 1)) * p.kbs + k);
-                        } else if (lane < 4) {
-                            cp_async_4(dst + BM + lane, sfb_src + k);
+                if constexpr (MODE == kKGrouped) {
+                    // Patches of KG_PATCH consecutive K blocks: lane (r, kk) loads the scales of rows /
+                    // columns r, r + 8, ... for the patch's K block kk, so that each load instruction reads
+                    // 8 rows x 16 contiguous bytes instead of 32 scattered words; each lane then arrives
+                    // on every slot of the patch, which completes when all of the patch has landed.
+                    const int kk = lane & (KG_PATCH - 1), rc = lane / KG_PATCH;
+                    for (int kb = 0; kb < ti.nkb;) {
+                        const int np = min(KG_PATCH, ti.nkb - kb);
+                        bool got = true;
+                        int s = slot;
+                        uint32_t ph = sphase;
+                        for (int j = 0; j < np; ++j) {
+                            got = got && (mbar_try_wait(&scale_empty_bar[s], ph ^ 1u) ||
+                                          wait_backoff(&scale_empty_bar[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns));
+                            if (++s == C::SCALE_SLOTS) { s = 0; ph ^= 1u; }
                         }
-                        cp_async_arrive_noinc(&scale_full_bar[slot]);
-                        if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                        if (kk < np) {
+                            const int my = (slot + kk) % C::SCALE_SLOTS;
+                            float* dst = s_scales + my * C::SLOT_FLOATS;
+                            const int k = ti.kb0 + kb + kk;
+#pragma unroll 4
+                            for (int r = rc; r < BM; r += 32 / KG_PATCH)
+                                cp_async_4(dst + r, p.sfa + static_cast<size_t>(min(ti.a_row + r, a_rows_total - 1)) * p.kbs + k);
+#pragma unroll 4
+                            for (int c = rc; c < BN; c += 32 / KG_PATCH)
+                                cp_async_4(dst + BM + c, p.sfb + static_cast<size_t>(min(ti.n0 + c, p.n - 1)) * p.kbs + k);
+                        }
+                        for (int j = 0; j < np; ++j) {
+                            cp_async_arrive_noinc(&scale_full_bar[slot]);
+                            if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                        }
+                        kb += np;
                     }
-                    kb += take;
+                } else {
+                    for (int kb = 0; kb < ti.nkb;) {
+                        // as in the producer: a second slot is filled in the same pass if it is free already
+                        int s1 = slot + 1;
+                        uint32_t sp1 = sphase;
+                        if (s1 == C::SCALE_SLOTS) { s1 = 0; sp1 ^= 1u; }
+                        const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
+                        const bool f0 = mbar_try_wait(&scale_empty_bar[slot], sphase ^ 1u);
+                        const bool f1 = more && mbar_test_wait(&scale_empty_bar[s1], sp1 ^ 1u);
+                        // the stager runs several slots ahead, so it waits with a sleeping backoff (the
+                        // wake-up latency is hidden; polling would take issue slots from the epilogue warps
+                        // of its sub-partition)
+                        const bool got = f0 || wait_backoff(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                        const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
+                        for (int j = 0; j < take; ++j) {
+                            const int k = kb + j;
+                            float* dst = s_scales + slot * C::SLOT_FLOATS;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + k);
+                            if (lane < 4) {
+                                cp_async_4(dst + BM + lane, sfb_src + k);
+                            }
+                            cp_async_arrive_noinc(&scale_full_bar[slot]);
+                            if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
+                        }
+                        kb += take;
+                    }
                 }
                 if (!ok) break;
             }
@@ -725,7 +762,6 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         uint32_t xphase = 0;                   // narrow-tile exchange rounds so far (parity)
         int acc = 0, slot = 0;
         uint32_t acc_phase = 0, sphase = 0;
-        uint32_t store_round = 0;              // TMA-store boxes issued so far (picks the staging slot)
         bool ok = true;
 
         for (int t = unit; t < num_tiles && ok; t += num_units) {
@@ -736,8 +772,8 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             const int bidx = cstart / 128 - ti.n0 / 128;
             const int split = (128 * (cstart / 128 + 1) - cstart) / 16;   // chunks before the next block
 
-            // the k-grouped output is accumulated by the TMA's add at the tile's end, so every layout
-            // starts the tile's sum at zero
+            // the k-grouped output is added into D at the tile's end, so every layout starts the tile's
+            // sum at zero
             float accum[COLS];
 #pragma unroll
             for (int j = 0; j < COLS; ++j) accum[j] = 0.f;
@@ -973,30 +1009,35 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             }
             // ---- store this CTA's rows of the tile
             if (MODE == kKGrouped) {
-                // D[g] += tile: FP32 boxes of 32 rows x 8 columns, added element-wise by the TMA (one
-                // add per element, so the result does not depend on timing), or stored (overwriting
-                // form); the three-dimensional map [G][M][N] skips rows past M and columns past N
-                uint8_t* wbuf = s_store + ew * C::STORE_WARP_BYTES;
-                const int y = ti.m0 + q * 32;
-                const int sw = (lane >> 2) & 1;
+                // D[g] += tile (or D[g] = tile in the overwriting form), 16 columns at a time: each lane
+                // parks its row's 16 sums in the warp's buffer ([32 rows][16 floats], 16-byte chunks
+                // swizzled by row pair, conflict-free both ways), then every lane takes one 16-byte piece
+                // of a row, so that one instruction covers 8 rows x 64 contiguous bytes. The adds are
+                // vector reductions at L2: one add per element, so the result does not depend on timing.
+                float* tb = reinterpret_cast<float*>(s_store + ew * C::STORE_WARP_BYTES);
+                float* dg = static_cast<float*>(p.d) + static_cast<size_t>(ti.g) * p.rows * p.n;
+                const int y0 = ti.m0 + q * 32;
+                const int pc = lane & 3;          // the 16-byte piece of a row this lane moves
 #pragma unroll
-                for (int c = 0; c < COLS / 8; ++c) {
-                    uint8_t* half = wbuf + (store_round % C::STORE_SLOTS) * 1024;
-                    ++store_round;
-                    if (lane == 0) bulk_wait_read_n<C::STORE_SLOTS - 1>();
+                for (int c = 0; c < COLS / 16; ++c) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<float4*>(tb + lane * 16 + ((i ^ ((lane >> 1) & 3)) * 4)) =
+                            make_float4(accum[c * 16 + 4 * i], accum[c * 16 + 4 * i + 1],
+                                        accum[c * 16 + 4 * i + 2], accum[c * 16 + 4 * i + 3]);
                     __syncwarp();
-                    uint4* rowp = reinterpret_cast<uint4*>(half + lane * 32);
-                    rowp[sw] = make_uint4(__float_as_uint(accum[c * 8 + 0]), __float_as_uint(accum[c * 8 + 1]),
-                                          __float_as_uint(accum[c * 8 + 2]), __float_as_uint(accum[c * 8 + 3]));
-                    rowp[sw ^ 1] = make_uint4(__float_as_uint(accum[c * 8 + 4]), __float_as_uint(accum[c * 8 + 5]),
-                                              __float_as_uint(accum[c * 8 + 6]), __float_as_uint(accum[c * 8 + 7]));
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (p.overwrite) tma_store_3d(&tmap_d, half, cstart + c * 8, y, ti.g);
-                        else tma_reduce_add_3d(&tmap_d, half, cstart + c * 8, y, ti.g);
-                        bulk_commit();
+                    const int col = cstart + c * 16 + pc * 4;
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int rr = it * 8 + (lane >> 2);
+                        const float4 v = *reinterpret_cast<const float4*>(tb + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
+                        if (y0 + rr < p.rows && col < p.n) {
+                            float* dst = dg + static_cast<size_t>(y0 + rr) * p.n + col;
+                            if (p.overwrite) st_global_v4(dst, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
+                            else red_add_v4_f32(dst, v.x, v.y, v.z, v.w);
+                        }
                     }
+                    __syncwarp();
                 }
             } else if constexpr (C::FULL_STAGE) {
                 // BF16 out: the warp's 32 rows x COLS columns go to its staging boxes (32 x 32, 64 bytes a

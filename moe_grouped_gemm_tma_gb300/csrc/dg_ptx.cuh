@@ -116,22 +116,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                  : "memory");
 }
 
-// 3-D tiled store of a box from shared memory (bulk-group completion); elements outside the tensor
-// are not written.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
-                 ::"l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
-                 : "memory");
-}
-
-// Element-wise add of a shared-memory box into global memory (the add happens in L2); the element
-// type is the tensor map's. Elements outside the tensor are skipped.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
-    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-                 ::"l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
-                 : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until the bulk stores issued by this thread have finished reading shared memory.
@@ -448,6 +432,11 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
         : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
         : "memory");
     return out != 0;
+}
+
+// p[0..3] += (a, b, c, d): a vector reduction performed at L2 (relaxed, GPU scope); p 16-byte aligned
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
