@@ -177,7 +177,7 @@ constexpr Spec kMaskedSpecs1[] = {{64, 1}, {128, 1}, {192, 1}, {256, 1}};
 constexpr Spec kMaskedSpecs2[] = {{128, 2}, {256, 2}};
 constexpr Spec kKGroupedSpecs1[] = {{128, 1}, {192, 1}, {224, 1}, {256, 1}};
 // automatic k-grouped choice: its per-column promotion makes tiles wider than 192 slower
-constexpr Spec kKGroupedAuto1[] = {{128, 1}, {192, 1}};
+constexpr Spec kKGroupedAuto1[] = {{128, 1}, {192, 1}, {256, 1}};
 constexpr Spec kKGroupedSpecs2[] = {{128, 2}};
 
 // Pick BN minimising waves * (BN + per-tile overhead), ties to the larger BN: the time of one wave of
