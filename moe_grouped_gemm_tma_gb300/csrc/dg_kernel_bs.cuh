@@ -79,9 +79,14 @@ struct CfgBS {
 // the scale writers the pacing loop: 476 against 358 us on 4096 x 7168 x 16384.)
 __device__ __forceinline__ uint32_t ue8m0x4(float s, uint32_t& bad) {
     const uint32_t bits = __float_as_uint(s);
-    // sign or mantissa bits, zero, or the all-ones exponent (infinity or NaN, which UE8M0 cannot hold)
-    bad |= (bits & 0x807FFFFFu) | static_cast<uint32_t>(bits == 0u) | static_cast<uint32_t>((bits >> 23) == 0xFFu);
+    // sign or mantissa bits; a zero exponent (bits - 2^23 borrows into the sign bit); the all-ones
+    // exponent of infinity and NaN, which UE8M0 cannot hold (bits + 2^23 carries into the sign bit)
+    bad |= (bits & 0x807FFFFFu) | ((bits - 0x00800000u) & 0x80000000u) | ((bits + 0x00800000u) & 0x80000000u);
     return ((bits >> 23) & 0xFFu) * 0x01010101u;
+}
+
+__device__ __forceinline__ uint32_t pick4u(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3, int i) {
+    return i == 0 ? e0 : (i == 1 ? e1 : (i == 2 ? e2 : e3));
 }
 
 template <int BN, int PAIR>
@@ -342,8 +347,11 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                         vb[j] = (j < BN / 32) ? ((__float_as_uint(pick4(b4, bidx[j])) >> sh) & 0xFFu) * 0x01010101u : 0u;
                 } else {
                     va = ue8m0x4(sl[q * 32 + lane], bad);
+                    // the (at most four) 128-column blocks' exponents, converted once and picked per column
+                    const uint32_t e0 = ue8m0x4(b4.x, bad), e1 = ue8m0x4(b4.y, bad);
+                    const uint32_t e2 = ue8m0x4(b4.z, bad), e3 = ue8m0x4(b4.w, bad);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? ue8m0x4(pick4(b4, bidx[j]), bad) : 0u;
+                    for (int j = 0; j < 8; ++j) vb[j] = (j < BN / 32) ? pick4u(e0, e1, e2, e3, bidx[j]) : 0u;
                 }
                 const uint32_t col = static_cast<uint32_t>(C::SF_COL0 + slot * C::SLOT_COLS);
                 // A's exponent in the slot's first eight columns: the MMA reads row m's from column m / 32
