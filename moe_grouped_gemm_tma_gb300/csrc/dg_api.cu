@@ -162,11 +162,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // Specialisations per layout: (BN, PAIR); each must be instantiated in the matching dg_inst_*.cu.
-// outs = 1 selects the short-K form with whole-tile output staging (Cfg's OUTS; normal layout, BN=256,
-// single CTA only).
 struct Spec {
     int bn, pair;
-    int outs = 0;
 };
 constexpr Spec kNormalSpecs1[] = {{64, 1}, {96, 1}, {128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
 constexpr Spec kNormalSpecs2[] = {{128, 2}, {160, 2}, {192, 2}, {224, 2}, {256, 2}};
@@ -271,7 +268,6 @@ cudaError_t launch_spec(Spec sp, const Launch& L);
 
 template <>
 cudaError_t launch_spec<kNormal>(Spec sp, const Launch& L) {
-    if (sp.outs) return (sp.bn == 256 && sp.pair == 1) ? launch<kNormal, 256, 1, 1>(L) : cudaErrorInvalidValue;
     DG_CASE(kNormal, 64, 1) DG_CASE(kNormal, 96, 1) DG_CASE(kNormal, 128, 1) DG_CASE(kNormal, 160, 1)
     DG_CASE(kNormal, 192, 1) DG_CASE(kNormal, 224, 1) DG_CASE(kNormal, 256, 1)
     DG_CASE(kNormal, 128, 2) DG_CASE(kNormal, 160, 2) DG_CASE(kNormal, 192, 2) DG_CASE(kNormal, 224, 2)
@@ -525,11 +521,6 @@ static dg_status gemm_impl(const uint8_t* A, const float* sfa, const uint8_t* B,
     // together) evict-first. Measured on 4096 x 7168 x 16384: DRAM traffic per launch 483 -> 355 MB
     // (algorithmic 243 MB), 330.6 -> 325.7 us; on K <= 7168 shapes it measured 0.5-1.5% slower.
     p.l2_hint = (!a_mn && !b_mn && K >= 8192) ? 1 : 0;
-    // Short K (at most 12 K blocks a tile): whole-tile output staging beside a 3-stage ring. Measured
-    // against the 4-stage form with 2 KB store buffers: 4096 x 32768 x 512 105.5 -> 88.9 us, 4096 x
-    // 24576 x 1536 147.1 -> 146.7 us; at K = 2048 0.5% slower, at K = 7168 11% (4096 x 2112) and at
-    // K = 16384 18% slower.
-    if (sp.bn == 256 && sp.pair == 1 && split == 1 && K <= 1536) sp.outs = 1;
     const int64_t tiles = static_cast<int64_t>(p.m_blocks) * p.n_blocks;
     if (tiles > INT32_MAX) return DG_UNSUPPORTED_SHAPE;
     p.tiles = static_cast<int>(tiles);

@@ -10,7 +10,6 @@ template cudaError_t launch<kNormal, 160, 1>(const Launch&);
 template cudaError_t launch<kNormal, 192, 1>(const Launch&);
 template cudaError_t launch<kNormal, 224, 1>(const Launch&);
 template cudaError_t launch<kNormal, 256, 1>(const Launch&);
-template cudaError_t launch<kNormal, 256, 1, 1>(const Launch&);
 template cudaError_t launch<kNormal, 128, 2>(const Launch&);
 template cudaError_t launch<kNormal, 160, 2>(const Launch&);
 template cudaError_t launch<kNormal, 192, 2>(const Launch&);

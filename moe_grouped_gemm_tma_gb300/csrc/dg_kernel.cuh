@@ -113,10 +113,7 @@ constexpr int ring_stages(int stage_bytes, int scale_bytes, int store_bytes, int
     return s;
 }
 
-// OUTS = 1: stage the whole BF16 output tile (TMA stores) beside a ring of at least three stages
-// instead of four; the launcher takes it for short K, where a tile's few K blocks cannot hide a
-// synchronous tile-end store (4096 x 32768 x 512: 105.5 -> 88.9 us) and a fourth stage buys nothing.
-template <int MODE, int BN, int PAIR, int OUTS = 0>
+template <int MODE, int BN, int PAIR>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
     static_assert(PAIR == 1 || PAIR == 2, "PAIR is 1 or 2");
@@ -163,7 +160,7 @@ struct Cfg {
     // 32 columns, written with plain stores. (Shared memory is kept small for the k-grouped layout: its
     // scale stager relies on what L1 keeps beside it.)
     static constexpr bool FULL_STAGE = MODE != kKGrouped && COLS % 32 == 0 &&
-        ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, BM * BN * 2, STATIC_RESERVE) >= (OUTS ? 3 : 4);
+        ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, BM * BN * 2, STATIC_RESERVE) >= 4;
     static constexpr int STORE_WARP_BYTES = FULL_STAGE ? 32 * COLS * 2 : 2048;
     static constexpr int STORE_BYTES = EPI_WARPS_C * STORE_WARP_BYTES;
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
@@ -390,11 +387,11 @@ __device__ __forceinline__ void promote_chunk(float (&accum)[COLS], const uint32
     }
 }
 
-template <int MODE, int BN, int PAIR, int OUTS = 0>
-__global__ void __launch_bounds__(Cfg<MODE, BN, PAIR, OUTS>::THREADS_C, 1)
+template <int MODE, int BN, int PAIR>
+__global__ void __launch_bounds__(Cfg<MODE, BN, PAIR>::THREADS_C, 1)
 dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ Params p) {
-    using C = Cfg<MODE, BN, PAIR, OUTS>;
+    using C = Cfg<MODE, BN, PAIR>;
     constexpr int STAGES = C::STAGES;
     constexpr int NACC = C::NACC;
     constexpr int COLS = C::COLS;

@@ -21,7 +21,7 @@ struct Launch {
     cudaStream_t stream;
 };
 
-template <int MODE, int BN, int PAIR, int OUTS = 0>
+template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L);
 
 // The block-scaled (UE8M0) normal GEMM (dg_inst_bs.cu).
@@ -48,10 +48,10 @@ unsigned long long take_armed_wait_fault();
 inline bool pdl_enabled() { return tune(DG_TUNE_PDL) != 0; }
 
 #ifdef DG_DEFINE_LAUNCH
-template <int MODE, int BN, int PAIR, int OUTS>
+template <int MODE, int BN, int PAIR>
 cudaError_t launch(const Launch& L) {
-    using C = Cfg<MODE, BN, PAIR, OUTS>;
-    auto kern = dg_gemm_kernel<MODE, BN, PAIR, OUTS>;
+    using C = Cfg<MODE, BN, PAIR>;
+    auto kern = dg_gemm_kernel<MODE, BN, PAIR>;
     // One-time set-up per device for this specialisation (the shared-memory attribute and the checks
     // below are per function and device; caching them keeps the per-call host cost low).
     static std::mutex mu;
