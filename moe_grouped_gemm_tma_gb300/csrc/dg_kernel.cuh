@@ -1063,8 +1063,15 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
+                        // boxes that lie wholly past the output's last row or column are not issued: a TMA
+                        // store is given only boxes that start inside the tensor
+                        const int y = ti.d_row + q * 32;
+                        const int out_rows = (MODE == kMasked) ? p.groups * p.rows : p.rows;
+                        if (y < out_rows) {
 #pragma unroll
-                        for (int r = 0; r < COLS / 32; ++r) tma_store_2d(&tmap_d, wbuf + r * 2048, cstart + r * 32, ti.d_row + q * 32);
+                            for (int r = 0; r < COLS / 32; ++r)
+                                if (cstart + r * 32 < p.n) tma_store_2d(&tmap_d, wbuf + r * 2048, cstart + r * 32, y);
+                        }
                         bulk_commit();
                     }
                 } else {

@@ -436,7 +436,8 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmap_d, half, ti.n0 + c * 16, y);
+                    // only boxes that start inside the output are issued (rows past M, columns past N)
+                    if (y < p.rows && ti.n0 + c * 16 < p.n) tma_store_2d(&tmap_d, half, ti.n0 + c * 16, y);
                     bulk_commit();
                 }
                 if (i + 1 < CH) tmem_ld_wait();

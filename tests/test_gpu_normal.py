@@ -52,6 +52,19 @@ def test_every_tile_shape(bn, pair, M, tune):
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn} pair={pair}")
 
 
+@pytest.mark.parametrize("bn,pair", [(64, 1), (128, 1), (192, 1), (256, 2)])
+@pytest.mark.parametrize("M", [40, 100])
+def test_output_boxes_past_the_last_row(bn, pair, M, tune):
+    # fewer rows than one tile, without split-K: the whole-tile staging issues only the TMA store boxes
+    # that start inside D (the others lie wholly past its last row)
+    tune(bn=bn)
+    tune(pair=pair)
+    tune(split=1)
+    c = I.make_normal(I.seed_for(1, 950 + bn + M), M, 1000, 512)
+    D = run_normal(c)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"BN={bn} pair={pair} M={M}")
+
+
 @pytest.mark.parametrize("split", [2, 4, 8])
 @pytest.mark.parametrize("M,N,K", [(64, 1000, 4096), (128, 2112, 1024), (100, 512, 3200)])
 def test_split_k(split, M, N, K, tune):

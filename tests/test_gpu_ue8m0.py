@@ -32,6 +32,17 @@ def test_ue8m0_parity(M, N, K, bn, tune):
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 BN={bn} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("bn", [0, 256])
+def test_ue8m0_rows_short_of_one_tile(bn, tune):
+    # 40 rows and 4 K blocks (no split-K): the output boxes of rows 40..127 are not issued
+    if bn:
+        tune(bn=bn)
+    c = I.make_normal(I.seed_for(7, 4040 + bn), 40, 1000, 512, pow2=True)
+    D = run_ue8m0(c.A, c.sfa, c.B, c.sfb, 40, 1000)
+    assert dg.dg_device_status() == 0
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"ue8m0 BN={bn} 40x1000x512")
+
+
 def test_ue8m0_integer_exact_bitwise():
     # values in {-1, 0, 1} and power-of-two scales 2^-2 .. 2^2 per block: every 32-element slice sums
     # exactly, every output is a multiple of 2^-4 below 2^13, so the FP32 accumulation is exact and the
