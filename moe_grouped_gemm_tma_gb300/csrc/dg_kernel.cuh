@@ -20,20 +20,22 @@
 //   warp 1      TMEM owner (512 columns) and, in the leader, the MMA issuer: one lane issues four
 //               MMAs (K = 32) per K block into one of NACC TMEM accumulators, then commits (to both
 //               CTAs of a pair) the stage's `empty` barrier and the accumulator's `tmem_full` barrier.
-//   warp 2      scale stager: per K block, cp.async copies of the block's sfa column (this CTA's 128
-//               rows) and the sfb values the tile needs into a SCALE_SLOTS-deep shared ring, running
-//               ahead of the epilogue so no scale load latency reaches it.
+//               Where the accumulators pair up (two of them, one K block per pass) warp 3 issues the
+//               odd accumulators' blocks and warp 1 the even ones.
+//   warp 2      scale stager (k-grouped layout and narrow tiles): cp.async copies of each K block's sfa
+//               column (this CTA's 128 rows) and of the sfb values the tile needs into a
+//               SCALE_SLOTS-deep shared ring, ahead of the epilogue; k-grouped tiles load patches of
+//               KG_PATCH K blocks per pass. Wide tiles of the other layouts read their scales directly.
 //   warps 4..11 promotion / epilogue (two warpgroups, registers raised with setmaxnreg): each thread
 //               owns one tile row (its TMEM lane). Per K block a thread reads the block partial out of
-//               TMEM, releases the accumulator (`tmem_empty` in the leader) as soon as its loads have
-//               completed, multiplies by sfa[m,kb] * sfb and adds into FP32 running sums (packed f32x2
-//               FMA), then releases the scale slot. Wide tiles: the warpgroups split the BN columns.
-//               Narrow tiles (BN <= 64): each warpgroup takes every other K block over all columns,
-//               and the two partial sums are exchanged once per tile through shared memory. At the
-//               end of a tile they round to BF16 and either stage the whole tile in shared memory for
-//               TMA stores that complete in the background (where that fits beside a four-stage ring)
-//               or write it with coalesced plain stores; the weight gradient is TMA-added in 32 x 8
-//               FP32 boxes.
+//               TMEM, releases the accumulator (`tmem_empty` in the leader) once its loads have
+//               completed, and adds partial * sfa[m,kb] * sfb into FP32 running sums (packed f32x2
+//               FMAs). Wide tiles: the warpgroups split the BN columns. Narrow tiles (BN <= 64): each
+//               warpgroup takes every other K block over all columns, and the two partial sums are
+//               exchanged once per tile through shared memory. At the end of a tile they round to BF16
+//               and either stage the whole tile in shared memory for TMA stores that complete in the
+//               background (where that fits beside a four-stage ring) or write it with coalesced plain
+//               stores; the weight gradient is added into D with coalesced FP32 vector reductions.
 // The MMA of K block kb+1.. overlaps the promotion of block kb (NACC accumulators in flight), and the
 // store of one tile overlaps the first MMAs of the next. Small-M GEMMs split K over a cluster of CTAs
 // and reduce the FP32 partials through distributed shared memory.

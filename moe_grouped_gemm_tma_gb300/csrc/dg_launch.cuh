@@ -14,7 +14,7 @@ namespace dg {
 struct Launch {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;
-    CUtensorMap tmap_d;     // the output for TMA stores: BF16 boxes, or the FP32 [G][M][N] gradient (TMA add)
+    CUtensorMap tmap_d;     // the BF16 output for TMA stores (unused by the k-grouped gradient)
     Params params;
     int units;          // work units wanted: tiles (single CTA) or tile pairs (CTA pairs)
     int sms;
