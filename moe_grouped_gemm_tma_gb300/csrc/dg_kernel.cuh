@@ -1017,7 +1017,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 // of a row, so that one instruction covers 8 rows x 64 contiguous bytes. The adds are
                 // vector reductions at L2: one add per element, so the result does not depend on timing.
                 float* tb = reinterpret_cast<float*>(s_store + ew * C::STORE_WARP_BYTES);
-                float* dg = static_cast<float*>(p.d) + static_cast<size_t>(ti.g) * p.rows * p.n;
+                float* d_g = static_cast<float*>(p.d) + static_cast<size_t>(ti.g) * p.rows * p.n;
                 const int y0 = ti.m0 + q * 32;
                 const int pc = lane & 3;          // the 16-byte piece of a row this lane moves
 #pragma unroll
@@ -1034,7 +1034,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         const int rr = it * 8 + (lane >> 2);
                         const float4 v = *reinterpret_cast<const float4*>(tb + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
                         if (y0 + rr < p.rows && col < p.n) {
-                            float* dst = dg + static_cast<size_t>(y0 + rr) * p.n + col;
+                            float* dst = d_g + static_cast<size_t>(y0 + rr) * p.n + col;
                             if (p.overwrite) st_global_v4(dst, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
                             else red_add_v4_f32(dst, v.x, v.y, v.z, v.w);
                         }
