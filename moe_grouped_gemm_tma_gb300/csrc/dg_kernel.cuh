@@ -228,12 +228,16 @@ __device__ __forceinline__ TileInfo decode_tile(const Params& p, int t, const in
     ti.kb0 = 0;
     ti.nkb = p.kbs;
     if (MODE == kNormal || MODE == kContiguous) {
-        // bands of group_m row blocks; within a band the row block varies fastest
+        // bands of group_m row blocks; within a band the row block varies fastest. Odd bands take the
+        // column blocks in reverse (serpentine), so a band starts on the B column blocks the previous
+        // band read last, which may still be in L2 (DRAM reads of 4096 x 7168 x 16384: 324.8 -> 318.2
+        // MB; 4096 x 24576 x 1536: 81.7 -> 69.3 MB).
         const int band_tiles = p.group_m * p.n_blocks;
         const int band = t / band_tiles, r = t - band * band_tiles;
         const int m_first = band * p.group_m;
         const int gm = min(p.group_m, p.m_blocks - m_first);
-        const int mb = m_first + r % gm, nb = r / gm;
+        const int mb = m_first + r % gm;
+        const int nb = (band & 1) ? (p.n_blocks - 1 - r / gm) : (r / gm);
         ti.m0 = mb * TILE_M + rank * BM;
         ti.n0 = nb * BN;
         ti.a_row = ti.m0;
