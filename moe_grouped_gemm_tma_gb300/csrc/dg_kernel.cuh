@@ -440,7 +440,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         // parameters, not data of the previous grid, so this may precede the dependency wait)
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
-        prefetch_tmap(&tmap_d);
+        if (MODE != kKGrouped) prefetch_tmap(&tmap_d);   // the gradient is added without a tensor map
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
