@@ -173,7 +173,7 @@ constexpr Spec kBlockScaledSpecs2[] = {{128, 2}, {256, 2}};
 // B stored MN-major is staged in whole 128-column boxes
 constexpr Spec kNormalSpecsBMN[] = {{128, 1}, {256, 1}};
 constexpr Spec kContiguousSpecs[] = {{128, 1}, {160, 1}, {192, 1}, {224, 1}, {256, 1}};
-constexpr Spec kMaskedSpecs1[] = {{64, 1}, {128, 1}, {192, 1}, {256, 1}};
+constexpr Spec kMaskedSpecs1[] = {{64, 1}, {128, 1}, {192, 1}, {224, 1}, {256, 1}};
 constexpr Spec kMaskedSpecs2[] = {{128, 2}, {256, 2}};
 constexpr Spec kKGroupedSpecs1[] = {{128, 1}, {192, 1}, {224, 1}, {256, 1}};
 // automatic k-grouped choice: its per-column promotion makes tiles wider than 192 slower
@@ -284,7 +284,7 @@ cudaError_t launch_spec<kContiguous>(Spec sp, const Launch& L) {
 
 template <>
 cudaError_t launch_spec<kMasked>(Spec sp, const Launch& L) {
-    DG_CASE(kMasked, 64, 1) DG_CASE(kMasked, 128, 1) DG_CASE(kMasked, 192, 1) DG_CASE(kMasked, 256, 1)
+    DG_CASE(kMasked, 64, 1) DG_CASE(kMasked, 128, 1) DG_CASE(kMasked, 192, 1) DG_CASE(kMasked, 224, 1) DG_CASE(kMasked, 256, 1)
     DG_CASE(kMasked, 128, 2) DG_CASE(kMasked, 256, 2)
     return cudaErrorInvalidValue;
 }

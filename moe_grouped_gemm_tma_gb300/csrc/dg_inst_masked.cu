@@ -6,6 +6,7 @@ namespace dg {
 template cudaError_t launch<kMasked, 64, 1>(const Launch&);
 template cudaError_t launch<kMasked, 128, 1>(const Launch&);
 template cudaError_t launch<kMasked, 192, 1>(const Launch&);
+template cudaError_t launch<kMasked, 224, 1>(const Launch&);
 template cudaError_t launch<kMasked, 256, 1>(const Launch&);
 template cudaError_t launch<kMasked, 128, 2>(const Launch&);
 template cudaError_t launch<kMasked, 256, 2>(const Launch&);

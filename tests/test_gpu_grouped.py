@@ -103,7 +103,7 @@ def test_masked_all_empty_and_over_max():
     _check_masked(c2, got, [128, 3])
 
 
-@pytest.mark.parametrize("bn,pair", [(64, 1), (128, 1), (192, 1), (256, 1), (128, 2), (256, 2)])
+@pytest.mark.parametrize("bn,pair", [(64, 1), (128, 1), (192, 1), (224, 1), (256, 1), (128, 2), (256, 2)])
 def test_masked_every_tile_shape(bn, pair, tune):
     tune(bn=bn)
     tune(pair=pair)
