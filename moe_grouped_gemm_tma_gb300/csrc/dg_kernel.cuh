@@ -27,10 +27,12 @@
 //               SCALE_SLOTS-deep shared ring, ahead of the epilogue; k-grouped tiles load patches of
 //               KG_PATCH K blocks per pass. Wide tiles of the other layouts read their scales directly.
 //   warps 4..11 promotion / epilogue (two warpgroups, registers raised with setmaxnreg): each thread
-//               owns one tile row (its TMEM lane). Per K block a thread reads the block partial out of
-//               TMEM, releases the accumulator (`tmem_empty` in the leader) once its loads have
-//               completed, and adds partial * sfa[m,kb] * sfb into FP32 running sums (packed f32x2
-//               FMAs). Wide tiles: the warpgroups split the BN columns. Narrow tiles (BN <= 64): each
+//               owns one tile row (its TMEM lane) -- in the k-grouped layout, 4 rows x 2 columns of every
+//               8-column group (the 16x256b TMEM load shape), so that it reads a quarter of the
+//               per-column scales. Per K block a thread reads the block partial out of TMEM, releases
+//               the accumulator (`tmem_empty` in the leader) once its loads have completed, and adds
+//               partial * sfa[m,kb] * sfb into FP32 running sums (packed f32x2 FMAs). Wide tiles: the
+//               warpgroups split the BN columns. Narrow tiles (BN <= 64): each
 //               warpgroup takes every other K block over all columns, and the two partial sums are
 //               exchanged once per tile through shared memory. At the end of a tile they round to BF16
 //               and either stage the whole tile in shared memory for TMA stores that complete in the
@@ -124,10 +126,14 @@ struct Cfg {
     static constexpr int B_ROWS = BN / PAIR;            // B rows staged by each CTA
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // scale slot: sfa of the CTA's 128 rows, then sfb: 4 block rows (from n0/128), or BN per-row values
-    // (k-grouped slots are padded by 8 floats, so that the stager's patch writes -- 8 rows or columns x
-    // 4 consecutive slots per instruction -- fall in distinct banks)
-    static constexpr int SB = (MODE == kKGrouped) ? BN + 8 : 4;
+    // scale slot: sfa of the CTA's 128 rows, then sfb: 4 block rows (from n0/128), or, k-grouped, BN
+    // per-column values in the epilogue's lane order: per warpgroup column block, four runs of KG_CS
+    // floats (lane class t%4: the two columns 2(t%4), 2(t%4)+1 of every 8-column group), each run padded
+    // so that the four classes' 16-byte reads fall in distinct banks (KG_CS / 4 odd); the slot is padded
+    // by 8 more floats, so that the stager's patch writes -- 8 consecutive positions x 4 consecutive slots
+    // per instruction -- fall in distinct banks
+    static constexpr int KG_CS = (BN / 8) + (((BN / 32) % 2 == 0) ? 4 : 0);
+    static constexpr int SB = (MODE == kKGrouped) ? 2 * 4 * KG_CS + 8 : 4;
     static constexpr int SLOT_FLOATS = BM + SB;
     // the k-grouped slots hold BN per-column values, so they get a shallower ring (eight: six would
     // leave room for a fifth operand stage at BN = 192, but the stager's scattered per-column loads
@@ -157,13 +163,13 @@ struct Cfg {
     // (each epilogue warp its 32 rows x COLS columns as boxes of 32 x 32 with the 64-byte swizzle),
     // written by TMA stores that the warp does not wait for until it stages its next tile (a tile's
     // 64 KB take the SM's store path several thousand cycles, which would otherwise stall promotion).
-    // Otherwise 2 KB per epilogue warp: for the k-grouped FP32 output a buffer of 32 rows x 16 columns
-    // that turns each lane's row into coalesced vector reductions; for BF16 out one buffer of 32 rows x
-    // 32 columns, written with plain stores. (Shared memory is kept small for the k-grouped layout: its
-    // scale stager relies on what L1 keeps beside it.)
+    // Otherwise, for BF16 out, 2 KB per epilogue warp: one buffer of 32 rows x 32 columns, written with
+    // plain stores. The k-grouped FP32 output needs none: lanes pair up their registers by shuffles into
+    // coalesced vector reductions. (Shared memory is kept small for the k-grouped layout: its scale
+    // stager relies on what L1 keeps beside it.)
     static constexpr bool FULL_STAGE = MODE != kKGrouped && COLS % 32 == 0 &&
         ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, BM * BN * 2, STATIC_RESERVE) >= 4;
-    static constexpr int STORE_WARP_BYTES = FULL_STAGE ? 32 * COLS * 2 : 2048;
+    static constexpr int STORE_WARP_BYTES = FULL_STAGE ? 32 * COLS * 2 : (MODE == kKGrouped ? 0 : 2048);
     static constexpr int STORE_BYTES = EPI_WARPS_C * STORE_WARP_BYTES;
     static constexpr int STAGES = ring_stages(STAGE_BYTES, SCALE_BYTES + XCHG_BYTES, STORE_BYTES, STATIC_RESERVE);
     static constexpr int NACC_FIT = TMEM_COLS / BN;
@@ -172,10 +178,9 @@ struct Cfg {
     static constexpr int STORE_OFF = ((XCHG_OFF + XCHG_BYTES + 1023) / 1024) * 1024;
     static constexpr int DYN_SMEM = 1024 + STORE_OFF + STORE_BYTES;
     static_assert(COLS % 16 == 0, "each epilogue warpgroup takes whole 16-column chunks");
+    static_assert(MODE != kKGrouped || (NWG == 2 && KG_CS >= COLS / 4 && (KG_CS / 4) % 2 == 1),
+                  "k-grouped scale runs: one per lane class, a quarter of a warpgroup's columns, odd in 16 bytes");
     static constexpr int CHUNKS = COLS / 16;   // 16-column TMEM loads per K block
-    // Epilogue TMEM loads per K block come in batches of EPI_GC chunks, each batch waited on once.
-    // Double-buffered (EPI_DB): batch g+1 is in flight while batch g is promoted. Single-buffered:
-    // larger batches in the same registers, so fewer load round trips per block.
     // Narrow tiles (four or more accumulators) and the k-grouped layout let the producer, the MMA issuer
     // and the scale stager take a second K block in the same pass of their loops when it is ready
     // already: a pass costs several hundred cycles of barrier round trips, more than the MMA of a narrow
@@ -197,8 +202,6 @@ struct Cfg {
     // warp idle, whose issue slots the epilogue warps of its sub-partition then get (per-block clock
     // stamps showed those warps releasing the accumulator last).
     static constexpr bool DIRECT_SCALES = !KPAR && MODE != kKGrouped;
-    static constexpr int EPI_GC = EPI_ONE ? CHUNKS : 2;   // (k-grouped at BN = 256: 1% faster than 1)
-    static constexpr bool EPI_DB = !EPI_ONE;
     // split-K partial sums: [128 rows][BN + 4] FP32 (padded rows: conflict-free 16-byte stores), in the
     // operand ring, which is idle once the tile's last MMA has completed
     static constexpr int PSTRIDE = BN + 4;
@@ -301,7 +304,11 @@ __device__ __forceinline__ void record_status(int* status, int code) { atomicCAS
 
 // Bounded mbarrier wait. Returns false when this CTA is aborting (this waiter timed out, or another
 // role did); the first waiter to time out records the status and raises the abort flag. `limit_ns` is
-// the launch's wait limit (0 = WAIT_LIMIT_NS).
+// the launch's wait limit (0 = WAIT_LIMIT_NS). Between checks of the flag and the clock the thread
+// waits in try_wait with a 1 us suspend hint, so that a waiting warp is suspended instead of polling:
+// a polling warp takes issue slots from the epilogue warps of its sub-partition (per-block clock stamps:
+// a control warp polling with plain try_wait delayed those warps' accumulator release by ~350 cycles
+// per K block; test_wait with a 32 ns sleep between polls, 0.5-1% slower than the suspend hint).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              int* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -309,33 +316,8 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > limit) {
-            *abort_flag = 1;
-            record_status(status, STATUS_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// Bounded wait for the control warps (TMA producer, MMA issuers): between polls the warp sleeps
-// briefly, so that a control warp waiting on a barrier takes no issue slots from the two epilogue warps
-// that share its sub-partition (per-block clock stamps: a control warp waiting with try_wait alone
-// delayed those warps' accumulator release by ~350 cycles per K block). Same result and bound as
-// wait_bounded; the reaction to a completed phase is at most one sleep later.
-__device__ __forceinline__ bool wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             int* status, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t limit = limit_ns ? limit_ns : WAIT_LIMIT_NS;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i) {
-            if (mbar_test_wait(bar, parity)) return true;
-            __nanosleep(32);
-        }
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_hint(bar, parity, 1000)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > limit) {
             *abort_flag = 1;
@@ -362,33 +344,39 @@ __device__ __forceinline__ float pick4(const float4& v, int i) {
 }
 
 // Promotion of one 16-column chunk c of a K block's partial sums r into the running sums:
-// acc += r * s (s = sfa * sfb of the chunk's 128-column block), or, with per-column scales (k-grouped),
-// acc += (r * scol[n]) * sa.
-template <int MODE, int COLS>
-__device__ __forceinline__ void promote_chunk(float (&accum)[COLS], const uint32_t* r, int c, float s, float sa,
-                                              const float* scol) {
-    if (MODE == kKGrouped) {
-        const float2 sa2 = make_float2(sa, sa);
+// acc += r * s (s = sfa * sfb of the chunk's 128-column block).
+template <int COLS>
+__device__ __forceinline__ void promote_chunk(float (&accum)[COLS], const uint32_t* r, int c, float s) {
+    const float2 s2 = make_float2(s, s);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            const float4 sv = *reinterpret_cast<const float4*>(scol + c * 16 + j);
-            float2 a0 = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
-            float2 a1 = make_float2(accum[c * 16 + j + 2], accum[c * 16 + j + 3]);
-            const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), make_float2(sv.x, sv.y));
-            const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), make_float2(sv.z, sv.w));
-            a0 = __ffma2_rn(p0, sa2, a0);
-            a1 = __ffma2_rn(p1, sa2, a1);
-            accum[c * 16 + j] = a0.x; accum[c * 16 + j + 1] = a0.y;
-            accum[c * 16 + j + 2] = a1.x; accum[c * 16 + j + 3] = a1.y;
-        }
-    } else {
-        const float2 s2 = make_float2(s, s);
+    for (int j = 0; j < 16; j += 2) {
+        float2 a = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
+        a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2, a);
+        accum[c * 16 + j] = a.x;
+        accum[c * 16 + j + 1] = a.y;
+    }
+}
+
+// k-grouped promotion of one 16-column chunk c (8-column groups 2c and 2c + 1) in the 16x256b register
+// layout: lo holds the lanes base .. base + 15 (the lane's rows 0 and 1), hi base + 16 .. base + 31
+// (rows 2 and 3); sv the lane's column scales (group 2c: x, y; group 2c + 1: z, w), sa its four row
+// scales. accum[(j * 4 + i) * 2 + e] += (P * sfb) * sfa for group j, row i, column e of the lane's pair.
+template <int COLS>
+__device__ __forceinline__ void promote_kg_chunk(float (&accum)[COLS], const uint32_t* lo, const uint32_t* hi, int c,
+                                                 const float4& sv, const float4& sa) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-            float2 a = make_float2(accum[c * 16 + j], accum[c * 16 + j + 1]);
-            a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), s2, a);
-            accum[c * 16 + j] = a.x;
-            accum[c * 16 + j + 1] = a.y;
+    for (int m = 0; m < 2; ++m) {
+        const float2 sb = m ? make_float2(sv.z, sv.w) : make_float2(sv.x, sv.y);
+        const int j = 2 * c + m;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t* w = (i < 2 ? lo : hi) + 4 * m + 2 * (i & 1);
+            const float s = i == 0 ? sa.x : (i == 1 ? sa.y : (i == 2 ? sa.z : sa.w));
+            float2 a = make_float2(accum[(j * 4 + i) * 2], accum[(j * 4 + i) * 2 + 1]);
+            const float2 pr = __fmul2_rn(make_float2(__uint_as_float(w[0]), __uint_as_float(w[1])), sb);
+            a = __ffma2_rn(pr, make_float2(s, s), a);
+            accum[(j * 4 + i) * 2] = a.x;
+            accum[(j * 4 + i) * 2 + 1] = a.y;
         }
     }
 }
@@ -534,7 +522,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
                     const bool f0 = mbar_try_wait(&empty_bar[stage], phase ^ 1u);
                     const bool f1 = more && mbar_test_wait(&empty_bar[s1], ph1 ^ 1u);
-                    const bool got = f0 || wait_backoff(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                    const bool got = f0 || wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
                     for (int j = 0; j < take; ++j) {
@@ -690,10 +678,13 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 const float* sfb_src = p.sfb + (static_cast<size_t>(ti.g) * p.sfb_rows + blk) * p.kbs + ti.kb0;
                 bool ok = true;
                 if constexpr (MODE == kKGrouped) {
-                    // Patches of KG_PATCH consecutive K blocks: lane (r, kk) loads the scales of rows /
-                    // columns r, r + 8, ... for the patch's K block kk, so that each load instruction reads
-                    // 8 rows x 16 contiguous bytes instead of 32 scattered words; each lane then arrives
-                    // on every slot of the patch, which completes when all of the patch has landed.
+                    // Patches of KG_PATCH consecutive K blocks: lane (r, kk) fills slot positions r, r + 8,
+                    // ... for the patch's K block kk, so that each load instruction reads 8 rows x 16
+                    // contiguous bytes instead of 32 scattered words; each lane then arrives on every slot
+                    // of the patch, which completes when all of the patch has landed. Positions are in the
+                    // epilogue's lane order: sfa position 32w + 4a + i holds row 32w + 8i + a, and the
+                    // sfb run of lane class cls in column block hh holds, at 2j + e, column
+                    // hh * COLS + 8j + 2cls + e.
                     const int kk = lane & (KG_PATCH - 1), rc = lane / KG_PATCH;
                     for (int kb = 0; kb < ti.nkb;) {
                         const int np = min(KG_PATCH, ti.nkb - kb);
@@ -702,7 +693,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         uint32_t ph = sphase;
                         for (int j = 0; j < np; ++j) {
                             got = got && (mbar_try_wait(&scale_empty_bar[s], ph ^ 1u) ||
-                                          wait_backoff(&scale_empty_bar[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns));
+                                          wait_bounded(&scale_empty_bar[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns));
                             if (++s == C::SCALE_SLOTS) { s = 0; ph ^= 1u; }
                         }
                         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -710,12 +701,33 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                             const int my = (slot + kk) % C::SCALE_SLOTS;
                             float* dst = s_scales + my * C::SLOT_FLOATS;
                             const int k = ti.kb0 + kb + kk;
+                            // sfa: lane rc fills positions rc + 8 it, i.e. rows ra + 32 (it / 4) + 2 (it % 4)
+                            const int ra = 8 * (rc & 3) + (rc >> 2);
+                            const int rmax = a_rows_total - 1 - ti.a_row;
+                            const float* sa_k = p.sfa + static_cast<size_t>(ti.a_row) * p.kbs + k;
 #pragma unroll 4
-                            for (int r = rc; r < BM; r += 32 / KG_PATCH)
-                                cp_async_4(dst + r, p.sfa + static_cast<size_t>(min(ti.a_row + r, a_rows_total - 1)) * p.kbs + k);
-#pragma unroll 4
-                            for (int c = rc; c < BN; c += 32 / KG_PATCH)
-                                cp_async_4(dst + BM + c, p.sfb + static_cast<size_t>(min(ti.n0 + c, p.n - 1)) * p.kbs + k);
+                            for (int it = 0; it < BM / 8; ++it) {
+                                const int r = min(ra + 32 * (it >> 2) + 2 * (it & 3), rmax);
+                                cp_async_4(dst + rc + 8 * it, sa_k + static_cast<size_t>(r) * p.kbs);
+                            }
+                            // sfb: lane rc fills positions rc + 8 j of every run (hh, cls), i.e. columns
+                            // cb + hh * COLS + 2 cls + 32 j
+                            constexpr int RUN = COLS / 4;
+                            const int cb = 8 * (rc >> 1) + (rc & 1);
+                            const int cmax = p.n - 1 - ti.n0;
+                            const float* sb_k = p.sfb + static_cast<size_t>(ti.n0) * p.kbs + k;
+#pragma unroll 1
+                            for (int run = 0; run < 8; ++run) {
+                                const int hh = run >> 2, cls = run & 3;
+#pragma unroll
+                                for (int j = 0; j < (RUN + 7) / 8; ++j) {
+                                    if (8 * j + 8 <= RUN || rc + 8 * j < RUN) {
+                                        const int c = min(cb + hh * COLS + 2 * cls + 32 * j, cmax);
+                                        cp_async_4(dst + BM + hh * 4 * C::KG_CS + cls * C::KG_CS + rc + 8 * j,
+                                                   sb_k + static_cast<size_t>(c) * p.kbs);
+                                    }
+                                }
+                            }
                         }
                         for (int j = 0; j < np; ++j) {
                             cp_async_arrive_noinc(&scale_full_bar[slot]);
@@ -732,10 +744,9 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         const bool more = C::KB_PAIRING && kb + 1 < ti.nkb;
                         const bool f0 = mbar_try_wait(&scale_empty_bar[slot], sphase ^ 1u);
                         const bool f1 = more && mbar_test_wait(&scale_empty_bar[s1], sp1 ^ 1u);
-                        // the stager runs several slots ahead, so it waits with a sleeping backoff (the
-                        // wake-up latency is hidden; polling would take issue slots from the epilogue warps
-                        // of its sub-partition)
-                        const bool got = f0 || wait_backoff(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                        // the stager runs several slots ahead, so the wake-up latency of its suspended wait
+                        // is hidden
+                        const bool got = f0 || wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                         const int take = __all_sync(0xffffffffu, f1) ? 2 : 1;
                         for (int j = 0; j < take; ++j) {
@@ -774,8 +785,6 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             const TileInfo ti = decode_tile<MODE, BN, PAIR>(p, t, s_prefix, rank, srank);
             if (!ti.valid) continue;
             const int cstart = ti.n0 + h * COLS;   // first output column of this thread
-            // sfb block rows of this thread's columns, as indices into the slot's 4 staged rows
-            const int bidx = cstart / 128 - ti.n0 / 128;
             const int split = (128 * (cstart / 128 + 1) - cstart) / 16;   // chunks before the next block
 
             // the k-grouped output is added into D at the tile's end, so every layout starts the tile's
@@ -817,7 +826,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     tmem_ld_wait();
                     if constexpr (H2 > 0) {
 #pragma unroll
-                        for (int c = 0; c < H1; ++c) promote_chunk<MODE, COLS>(accum, rb[c], c, (c < split) ? s0 : s1, sa, nullptr);
+                        for (int c = 0; c < H1; ++c) promote_chunk<COLS>(accum, rb[c], c, (c < split) ? s0 : s1);
 #pragma unroll
                         for (int c = 0; c < H2; ++c) tmem_ld_x16(taddr + (H1 + c) * 16, rb[c]);
                         tmem_ld_wait();
@@ -832,17 +841,26 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     if constexpr (H2 > 0) {
 #pragma unroll
                         for (int c = 0; c < H2; ++c)
-                            promote_chunk<MODE, COLS>(accum, rb[c], H1 + c, (H1 + c < split) ? s0 : s1, sa, nullptr);
+                            promote_chunk<COLS>(accum, rb[c], H1 + c, (H1 + c < split) ? s0 : s1);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < H1; ++c) promote_chunk<MODE, COLS>(accum, rb[c], c, (c < split) ? s0 : s1, sa, nullptr);
+                        for (int c = 0; c < H1; ++c) promote_chunk<COLS>(accum, rb[c], c, (c < split) ? s0 : s1);
                     }
                     if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
                 }
-            } else if constexpr (!C::KPAR) {
+            } else if constexpr (MODE == kKGrouped) {
+                // Per-column scales (weight gradient). The TMEM loads take the 16x256b shape: a lane holds
+                // rows t/4 + 8i (i = 0..3) of the warp's 32 and, of every 8-column group, columns 2(t%4)
+                // and 2(t%4) + 1, so it needs the column scales of only a quarter of its column block.
+                // The stager stores them in that order: one 16-byte read gives the lane's four row
+                // scales, one more its column scales of two groups. Loads in batches of two 16-column
+                // chunks, double-buffered; the accumulator is released once the last batch has landed,
+                // before its FMAs; the scale slot after the FMAs that read it.
+                constexpr int GC = 2;
+                constexpr int NG = (CHUNKS + GC - 1) / GC;
+                const float* sa_src = s_scales + q * 32 + (lane >> 2) * 4;
+                const float* sb_src = s_scales + BM + h * 4 * C::KG_CS + (lane & 3) * C::KG_CS;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    // both barriers are probed at once (each try_wait is a round trip to shared memory);
-                    // only an incomplete one falls back to the bounded waits
                     bool got = (static_cast<unsigned>(mbar_try_wait(&tmem_full_bar[acc], acc_phase)) &
                                 static_cast<unsigned>(mbar_try_wait(&scale_full_bar[slot], sphase))) != 0u;
                     if (!got)
@@ -851,43 +869,28 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t taddr = lane_addr + static_cast<uint32_t>(acc * BN);
-                    const float* sl = s_scales + slot * C::SLOT_FLOATS;
-                    const float sa = sl[row_in_tile];
-                    float s0 = 0.f, s1 = 0.f;
-                    if (MODE != kKGrouped) {
-                        const float4 b4 = *reinterpret_cast<const float4*>(sl + BM);
-                        s0 = sa * pick4(b4, bidx);
-                        s1 = sa * pick4(b4, bidx + 1 < 4 ? bidx + 1 : 3);
-                    }
-                    const float* scol = sl + BM + h * COLS;   // k-grouped per-column scales
-
-                    // TMEM loads and promotion in batches of GC chunks (see Cfg). The accumulator is released
-                    // right after its last load has completed, before the last batch's FMAs; the scale slot
-                    // after the FMAs that read it.
-                    constexpr int GC = C::EPI_GC;
-                    constexpr bool DB = C::EPI_DB;
-                    constexpr int NG = (CHUNKS + GC - 1) / GC;
-                    uint32_t rb[DB ? 2 : 1][GC][16];
-                    if (DB) {
+                    const float4 sa4 = *reinterpret_cast<const float4*>(sa_src + slot * C::SLOT_FLOATS);
+                    const float4* sb4 = reinterpret_cast<const float4*>(sb_src + slot * C::SLOT_FLOATS);
+                    uint32_t rb[2][2][GC * 8];   // [buffer][lane half][chunk * 8 + word]
 #pragma unroll
-                        for (int cc = 0; cc < GC; ++cc)
-                            if (cc < CHUNKS) tmem_ld_x16(taddr + cc * 16, rb[0][cc]);
-                        tmem_ld_wait();
-                    }
+                    for (int cc = 0; cc < GC; ++cc)
+                        if (cc < CHUNKS) {
+                            tmem_ld_16x256b_x2(taddr + cc * 16, &rb[0][0][cc * 8]);
+                            tmem_ld_16x256b_x2(taddr + (16u << 16) + cc * 16, &rb[0][1][cc * 8]);
+                        }
+                    tmem_ld_wait();
 #pragma unroll
                     for (int g = 0; g < NG; ++g) {
-                        const int b = DB ? (g & 1) : 0;
-                        if (!DB) {
+                        const int b = g & 1;
+                        if (g + 1 < NG) {
 #pragma unroll
                             for (int cc = 0; cc < GC; ++cc)
-                                if (g * GC + cc < CHUNKS) tmem_ld_x16(taddr + (g * GC + cc) * 16, rb[0][cc]);
-                            tmem_ld_wait();
-                        } else if (g + 1 < NG) {
-#pragma unroll
-                            for (int cc = 0; cc < GC; ++cc)
-                                if ((g + 1) * GC + cc < CHUNKS) tmem_ld_x16(taddr + ((g + 1) * GC + cc) * 16, rb[b ^ 1][cc]);
-                        }
-                        if (g + 1 == NG) {
+                                if ((g + 1) * GC + cc < CHUNKS) {
+                                    const uint32_t col = static_cast<uint32_t>(((g + 1) * GC + cc) * 16);
+                                    tmem_ld_16x256b_x2(taddr + col, &rb[b ^ 1][0][cc * 8]);
+                                    tmem_ld_16x256b_x2(taddr + (16u << 16) + col, &rb[b ^ 1][1][cc * 8]);
+                                }
+                        } else {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) {
@@ -900,9 +903,9 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         for (int cc = 0; cc < GC; ++cc) {
                             const int c = GC * g + cc;
                             if (c >= CHUNKS) break;
-                            promote_chunk<MODE, COLS>(accum, rb[b][cc], c, (c < split) ? s0 : s1, sa, scol);
+                            promote_kg_chunk<COLS>(accum, &rb[b][0][cc * 8], &rb[b][1][cc * 8], c, sb4[c], sa4);
                         }
-                        if (DB && g + 1 < NG) tmem_ld_wait();
+                        if (g + 1 < NG) tmem_ld_wait();
                     }
                     // every lane has read its scales (the FMAs above used them)
                     __syncwarp();
@@ -911,9 +914,9 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     if (++slot == C::SCALE_SLOTS) { slot = 0; sphase ^= 1u; }
                 }
             } else {
-                // all BN columns of every other K block (this warpgroup's parity); outside the k-grouped
-                // layout the columns lie in one 128-column sfb block (BN divides 128, n0 is a multiple
-                // of BN), so one scale sfa * sfb serves the row
+                // all BN columns of every other K block (this warpgroup's parity); the columns lie in one
+                // 128-column sfb block (BN divides 128, n0 is a multiple of BN), so one scale sfa * sfb
+                // serves the row
                 float accf[BN];
 #pragma unroll
                 for (int j = 0; j < BN; ++j) accf[j] = 0.f;
@@ -932,8 +935,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                         constexpr int NCH = BN / 16;
                         constexpr int LB = NCH < 4 ? NCH : 4;
                         const float* sl = s_scales + slot * C::SLOT_FLOATS;
-                        const float sa = sl[row_in_tile];
-                        const float sab = (MODE == kKGrouped) ? 0.f : sa * sl[BM];
+                        const float sab = sl[row_in_tile] * sl[BM];
 #pragma unroll
                         for (int b = 0; b < NCH / LB; ++b) {
                             uint32_t rb[LB][16];
@@ -950,7 +952,7 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                                 }
                             }
 #pragma unroll
-                            for (int c = 0; c < LB; ++c) promote_chunk<MODE, BN>(accf, rb[c], b * LB + c, sab, sa, sl + BM);
+                            for (int c = 0; c < LB; ++c) promote_chunk<BN>(accf, rb[c], b * LB + c, sab);
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&scale_empty_bar[slot]);
@@ -1014,36 +1016,35 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                 continue;
             }
             // ---- store this CTA's rows of the tile
-            if (MODE == kKGrouped) {
-                // D[g] += tile (or D[g] = tile in the overwriting form), 16 columns at a time: each lane
-                // parks its row's 16 sums in the warp's buffer ([32 rows][16 floats], 16-byte chunks
-                // swizzled by row pair, conflict-free both ways), then every lane takes one 16-byte piece
-                // of a row, so that one instruction covers 8 rows x 64 contiguous bytes. The adds are
-                // vector reductions at L2: one add per element, so the result does not depend on timing.
-                float* tb = reinterpret_cast<float*>(s_store + ew * C::STORE_WARP_BYTES);
+            if constexpr (MODE == kKGrouped) {
+                // D[g] += tile (or D[g] = tile in the overwriting form). Per 16-column chunk and row i, the
+                // lanes of a class pair (t, t ^ 1) swap one column pair, so that each lane holds 4
+                // contiguous columns: the even lane of its group 2c, the odd lane of group 2c + 1. One
+                // instruction then covers 8 rows x 64 contiguous bytes. The adds are vector reductions
+                // at L2: one add per element, so the result does not depend on timing.
                 float* d_g = static_cast<float*>(p.d) + static_cast<size_t>(ti.g) * p.rows * p.n;
-                const int y0 = ti.m0 + q * 32;
-                const int pc = lane & 3;          // the 16-byte piece of a row this lane moves
+                const int y0 = ti.m0 + q * 32 + (lane >> 2);
+                const bool odd = (lane & 1) != 0;
+                const int coff = odd ? 8 + 2 * ((lane & 3) - 1) : 2 * (lane & 3);
 #pragma unroll
-                for (int c = 0; c < COLS / 16; ++c) {
+                for (int c = 0; c < CHUNKS; ++c) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        *reinterpret_cast<float4*>(tb + lane * 16 + ((i ^ ((lane >> 1) & 3)) * 4)) =
-                            make_float4(accum[c * 16 + 4 * i], accum[c * 16 + 4 * i + 1],
-                                        accum[c * 16 + 4 * i + 2], accum[c * 16 + 4 * i + 3]);
-                    __syncwarp();
-                    const int col = cstart + c * 16 + pc * 4;
-#pragma unroll
-                    for (int it = 0; it < 4; ++it) {
-                        const int rr = it * 8 + (lane >> 2);
-                        const float4 v = *reinterpret_cast<const float4*>(tb + rr * 16 + ((pc ^ ((rr >> 1) & 3)) * 4));
-                        if (y0 + rr < p.rows && col < p.n) {
-                            float* dst = d_g + static_cast<size_t>(y0 + rr) * p.n + col;
+                    for (int i = 0; i < 4; ++i) {
+                        const int e0 = ((2 * c) * 4 + i) * 2, e1 = ((2 * c + 1) * 4 + i) * 2;
+                        const float s0 = odd ? accum[e0] : accum[e1];
+                        const float s1 = odd ? accum[e0 + 1] : accum[e1 + 1];
+                        const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+                        const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+                        const float4 v = odd ? make_float4(r0, r1, accum[e1], accum[e1 + 1])
+                                             : make_float4(accum[e0], accum[e0 + 1], r0, r1);
+                        const int row = y0 + 8 * i;
+                        const int col = cstart + c * 16 + coff;
+                        if (row < p.rows && col < p.n) {
+                            float* dst = d_g + static_cast<size_t>(row) * p.n + col;
                             if (p.overwrite) st_global_v4(dst, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w));
                             else red_add_v4_f32(dst, v.x, v.y, v.z, v.w);
                         }
                     }
-                    __syncwarp();
                 }
             } else if constexpr (C::FULL_STAGE) {
                 // BF16 out: the warp's 32 rows x COLS columns go to its staging boxes (32 x 32, 64 bytes a

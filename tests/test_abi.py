@@ -218,14 +218,14 @@ def test_kernels_report_failures_without_trapping():
 
 
 def test_every_device_loop_without_a_counted_bound_is_a_known_bounded_one():
-    # Waits in the kernels end: wait_bounded and wait_backoff give up after a time limit and raise the
-    # abort flag, drain_wait gives up after a shorter one; the only other open loops are the masked layout's binary
+    # Waits in the kernels end: wait_bounded gives up after a time limit and raises the abort flag (its
+    # suspended try_wait returns after at most its hint), drain_wait gives up after a shorter one; the only other open loops are the masked layout's binary
     # search (hi - lo halves each pass) and the host-side stage count. A new open loop must be added
     # here deliberately, with its bound.
     known = {
         "while (s > 1 && 1024 + ((s * stage_bytes + scale_bytes + 1023) / 1024) * 1024 + store_bytes + static_bytes > SMEM_LIMIT)",
         "while (hi - lo > 1) {",
-        "while (true) {",                              # wait_bounded / wait_backoff: exit on success, abort or time limit
+        "while (true) {",                              # wait_bounded: exit on success, abort or time limit
         "while (!mbar_try_wait(bar, parity))",         # drain_wait: exits on success or time limit
     }
     csrc = os.path.join(ROOT, "moe_grouped_gemm_tma_gb300", "csrc")
@@ -239,9 +239,11 @@ def test_every_device_loop_without_a_counted_bound_is_a_known_bounded_one():
     for f, code in found:
         assert code in known, (f, code)
     text = open(os.path.join(csrc, "dg_kernel.cuh"), encoding="utf-8").read()
-    body = text[text.index("bool wait_bounded("):text.index("bool wait_backoff(")]
-    assert "WAIT_LIMIT_NS" in body and "abort_flag" in body
-    body = text[text.index("bool wait_backoff("):text.index("void drain_wait(")]
+    body = text[text.index("bool wait_bounded("):text.index("void drain_wait(")]
     assert "WAIT_LIMIT_NS" in body and "abort_flag" in body and "STATUS_TIMEOUT" in body
+    # every suspended try_wait carries a finite hint (nanoseconds, an integer literal)
+    hints = re.findall(r"mbar_try_wait_hint\([^;]*?,\s*(\d+)\)", "".join(
+        open(os.path.join(csrc, f), encoding="utf-8").read() for f in sorted(os.listdir(csrc))))
+    assert hints and all(0 < int(h) <= 1_000_000 for h in hints), hints
     body = text[text.index("void drain_wait("):]
     assert "DRAIN_LIMIT_NS" in body[:400]
