@@ -872,24 +872,31 @@ dg_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
                     const float4 sa4 = *reinterpret_cast<const float4*>(sa_src + slot * C::SLOT_FLOATS);
                     const float4* sb4 = reinterpret_cast<const float4*>(sb_src + slot * C::SLOT_FLOATS);
                     uint32_t rb[2][2][GC * 8];   // [buffer][lane half][chunk * 8 + word]
+                    // a whole batch of 32 columns per load where every batch starts on a 32-column boundary
+                    // (column blocks of 64, 96 and 128), two 16-column loads otherwise
+                    constexpr bool X4 = (GC == 2) && (COLS % 32 == 0);
+                    auto load_batch = [&](int g, uint32_t (&dst)[2][GC * 8]) {
+                        if constexpr (X4) {
+                            const uint32_t col = static_cast<uint32_t>(g * 32);
+                            tmem_ld_16x256b_x4(taddr + col, &dst[0][0]);
+                            tmem_ld_16x256b_x4(taddr + (16u << 16) + col, &dst[1][0]);
+                        } else {
 #pragma unroll
-                    for (int cc = 0; cc < GC; ++cc)
-                        if (cc < CHUNKS) {
-                            tmem_ld_16x256b_x2(taddr + cc * 16, &rb[0][0][cc * 8]);
-                            tmem_ld_16x256b_x2(taddr + (16u << 16) + cc * 16, &rb[0][1][cc * 8]);
+                            for (int cc = 0; cc < GC; ++cc)
+                                if (g * GC + cc < CHUNKS) {
+                                    const uint32_t col = static_cast<uint32_t>((g * GC + cc) * 16);
+                                    tmem_ld_16x256b_x2(taddr + col, &dst[0][cc * 8]);
+                                    tmem_ld_16x256b_x2(taddr + (16u << 16) + col, &dst[1][cc * 8]);
+                                }
                         }
+                    };
+                    load_batch(0, rb[0]);
                     tmem_ld_wait();
 #pragma unroll
                     for (int g = 0; g < NG; ++g) {
                         const int b = g & 1;
                         if (g + 1 < NG) {
-#pragma unroll
-                            for (int cc = 0; cc < GC; ++cc)
-                                if ((g + 1) * GC + cc < CHUNKS) {
-                                    const uint32_t col = static_cast<uint32_t>(((g + 1) * GC + cc) * 16);
-                                    tmem_ld_16x256b_x2(taddr + col, &rb[b ^ 1][0][cc * 8]);
-                                    tmem_ld_16x256b_x2(taddr + (16u << 16) + col, &rb[b ^ 1][1][cc * 8]);
-                                }
+                            load_batch(g + 1, rb[b ^ 1]);
                         } else {
                             tc_fence_before();
                             __syncwarp();
