@@ -222,6 +222,20 @@ def test_dense_wgrad_parity(M, N, K, accumulate):
     check_f32(D.cpu().numpy(), want, f"dense wgrad accumulate={accumulate}")
 
 
+@pytest.mark.parametrize("bn", [128, 192, 224, 256])
+def test_dense_wgrad_overwrite_every_tile_width(bn, tune):
+    # the overwriting form at every tile width: 32-column TMEM load batches where the warpgroup's columns
+    # start on a 32-column boundary, 16-column ones at BN = 224; ragged M and N (N % 16 == 8)
+    tune(bn=bn)
+    M, N, K = 200, 264, 512
+    c = I.make_kgrouped(I.seed_for(5, bn), 1, M, N, [K])
+    D = torch.full((M, N), float("nan"), device="cuda")
+    dg.dg_wgrad_fp8_nt(dev(c.A), dev(c.sfa), dev(c.B), dev(c.sfb), D, accumulate=False)
+    assert dg.dg_device_status() == 0
+    want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, [K], torch.zeros(1, M, N))[0]
+    check_f32(D.cpu().numpy(), want, f"dense wgrad overwrite bn={bn}")
+
+
 def test_dense_wgrad_k_zero():
     M, N = 130, 64
     D = torch.full((M, N), 3.0, device="cuda")
