@@ -295,8 +295,8 @@ dg_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 const bool got = wait_bounded(&scale_empty_bar[slot], sphase ^ 1u, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 float* dst = s_scales + slot * C::SLOT_FLOATS;
-#pragma unroll
                 const int kidx = p.sf_packed ? ((ti.kb0 + kb) >> 2) : (ti.kb0 + kb);
+#pragma unroll
                 for (int i = 0; i < 4; ++i) cp_async_4(dst + lane + 32 * i, sfa_rows[i] + kidx);
                 if (lane < 4) cp_async_4(dst + BM + lane, sfb_src + kidx);
                 cp_async_arrive_noinc(&scale_full_bar[slot]);
