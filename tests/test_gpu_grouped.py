@@ -184,6 +184,25 @@ def test_kgrouped_small_full_parity(ks, M, N, bn, pair, tune):
             np.testing.assert_array_equal(got[g], c.D_in[g].numpy())
 
 
+@pytest.mark.parametrize("bn", [0, 224])
+@pytest.mark.parametrize("G,M,N,seed", [(32, 136, 200, 1), (128, 128, 64, 2)])
+def test_kgrouped_many_short_experts(G, M, N, seed, bn, tune):
+    # many experts with K windows of 0-3 blocks: scale patches shorter than four K blocks, windows that
+    # start at any K block, empty experts, up to the largest expert count the call takes
+    if bn:
+        tune(bn=bn)
+    rng = np.random.default_rng(seed)
+    ks = [int(k) for k in rng.integers(0, 4, size=G) * 128]
+    ks[0] = max(ks[0], 128)
+    c = I.make_kgrouped(I.seed_for(4, 1000 + seed), G, M, N, ks)
+    got = run_kgrouped(c)
+    want = O.k_grouped_wgrad(c.A, c.sfa, c.B, c.sfb, c.ks, c.D_in)
+    for g in range(G):
+        check_f32(got[g], want[g], f"k-grouped G={G} g={g}")
+        if ks[g] == 0:
+            np.testing.assert_array_equal(got[g], c.D_in[g].numpy())
+
+
 def test_kgrouped_integer_exact_bitwise():
     rng = np.random.default_rng(9)
     M, N, ks = 256, 256, [256, 128]
