@@ -93,6 +93,19 @@ def test_masked_small_full_parity_and_untouched_rows(G, max_m, masked, N, K):
     _check_masked(c, got, masked)
 
 
+@pytest.mark.parametrize("kernel", ["standard", "decode"])
+def test_masked_largest_expert_count(kernel, tune):
+    # the largest expert count the call takes (1024): the device-side tile count and its prefix scan over
+    # every expert, with empty experts and experts at max_m among them
+    tune(swap=1 if kernel == "decode" else 0)
+    G, max_m, N, K = 1024, 32, 128, 256
+    rng = np.random.default_rng(11)
+    masked = [int(x) for x in rng.integers(0, max_m + 1, size=G)]
+    c = I.make_masked(I.seed_for(3, 7000), G, max_m, N, K, masked)
+    got = run_masked(c, expected_m=16)
+    _check_masked(c, got, masked)
+
+
 def test_masked_all_empty_and_over_max():
     c = I.make_masked(I.seed_for(3, 1), 2, 128, 256, 256, [0, 0])
     got = run_masked(c)
