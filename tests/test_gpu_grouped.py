@@ -35,6 +35,19 @@ def test_contiguous_small_full_parity(G, group_m, N, K):
     check_bf16(got[valid], want[valid], f"contiguous G={G}")
 
 
+@pytest.mark.parametrize("bn", [128, 160, 192, 224, 256])
+def test_contiguous_every_tile_width(bn, tune):
+    # every tile width the contiguous layout takes, against a ragged N (264: a partial last column block
+    # at every width) and experts whose last row block is partly padding
+    tune(bn=bn)
+    G, group_m, N, K = 3, [130, 0, 77], 264, 384
+    c = I.make_contiguous(I.seed_for(2, 600 + bn), G, N, K, group_m)
+    got = run_contiguous(c)
+    valid = c.m_indices.numpy() >= 0
+    want = O.m_grouped_contiguous(c.A, c.sfa, c.B, c.sfb, c.m_indices)
+    check_bf16(got[valid], want[valid], f"contiguous bn={bn}")
+
+
 def test_contiguous_skips_blocks_that_start_with_padding():
     c = I.make_contiguous(I.seed_for(2, 5), 2, 256, 256, [128, 128])
     mi = c.m_indices.clone()
