@@ -32,6 +32,18 @@ def test_layout_parity(M, N, K, a_mn, b_mn):
     check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"a_mn={a_mn} b_mn={b_mn} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("a_mn,b_mn,bn", [(a, b, bn) for (a, b) in LAYOUTS for bn in (128, 256)] +
+                         [(True, False, bn) for bn in (64, 192, 224)])
+def test_layout_every_tile_width(a_mn, b_mn, bn, tune):
+    # every layout at the tile widths it takes (MN-major B: whole 128-column boxes, so 128 and 256; an
+    # MN-major A alone takes every width); ragged M and N
+    tune(bn=bn)
+    M, N, K = 208, 272, 384
+    c = I.make_normal(I.seed_for(6, 5000 + bn), M, N, K)
+    D = run_layout(c.A, c.sfa, c.B, c.sfb, M, N, a_mn, b_mn)
+    check_bf16(bf16_bits(D), O.gemm_fp8_nt(c.A, c.sfa, c.B, c.sfb), f"a_mn={a_mn} b_mn={b_mn} bn={bn}")
+
+
 @pytest.mark.parametrize("a_mn,b_mn", LAYOUTS)
 def test_layout_integer_exact_bitwise(a_mn, b_mn):
     # unit scales and values in {-1, 0, 1}: every output is an integer <= 256, exact in BF16
